@@ -1,0 +1,571 @@
+// fab_bwd_tc.cu -- the attention backward main kernel on the fifth-generation
+// tensor cores (tcgen05.mma, accumulators in tensor memory, operands staged by
+// TMA in 128-byte-swizzled shared memory).  bf16 inputs, D = DK = DV in
+// {64, 128}, f32 accumulation, f32 packed output.
+//
+// Math (labml "Flash Attention", "Backward pass"; ggmlR attn_ref for the mask
+// and scale): with S = scale * Q K^T + mask, P = exp(S - LSE) (the saved row
+// log-sum-exp), dV = P^T dO, dP = dO V^T, dS = P * (dP - D), dQ = scale dS K,
+// dK = scale dS^T Q.  D_i = dO_i . O_i comes from the preprocess kernel.
+//
+// Decomposition: one CTA per (key tile of BM = 128 keys, key/value head,
+// batch).  The key/value tile stays in shared memory; the CTA walks every
+// query head of the GQA group and every query tile of BQ = 64 queries
+// (skipping tiles a top-left causal mask empties), so dK and dV of the group
+// accumulate in tensor memory without atomics.  dQ tiles are reduced into the
+// packed dQ slice (zeroed beforehand) with bulk async f32 reductions.
+//
+// Per query tile, all in the transposed ("key rows") orientation so that one
+// thread owns one key row of every tensor-memory tile:
+//   S^T  = K  Q^T     [BM x BQ]  A = K (smem, K-major),  B = Q (smem, K-major)
+//   dP^T = V  dO^T    [BM x BQ]  A = V,                  B = dO
+//   P^T  = exp2(S^T * scale*log2e + mask*log2e - LSE*log2e)  -> bf16, tmem
+//   dV  += P^T dO     [BM x D]   A = P^T (tmem),         B = dO (smem, MN-major)
+//   dS^T = P^T * (dP^T - D)      -> bf16, tmem and smem
+//   dK  += dS^T Q     [BM x D]   A = dS^T (tmem),        B = Q (smem, MN-major)
+//   dQ^T = K^T dS^T   [D x BQ]   A = K (smem, MN-major), B = dS^T (smem, MN-major)
+// For D = 64 the dQ^T product runs with M = 128 against a zero-filled second
+// half of A, so every product uses the 128-lane accumulator layout.
+//
+// Warp roles (320 threads): warp 0 loads tiles with TMA (and the tile's LSE
+// and D rows); warp 1 allocates tensor memory and one lane issues every MMA;
+// warps 2-5 turn S and dP into P and dS (thread = key row); warps 6-9 drain
+// dQ^T (thread = feature row) into shared memory and issue the reductions.
+// All hand-offs are mbarriers; every wait is bounded (see fab_device.cuh).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fab.h"
+#include "fab_device.cuh"
+#include "fab_internal.h"
+
+namespace fab {
+namespace {
+
+__device__ uint32_t g_err_tc;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kThreads = 320;
+
+template <int D>
+struct Cfg {
+  static constexpr int BM = 128;  // keys per CTA (tensor-memory lanes)
+  static constexpr int BQ = 64;   // queries per step
+  static constexpr int STAGES = 2;
+  static constexpr int ATOMS = D / 64;  // 128-byte swizzle atoms along D
+  static constexpr uint32_t KV_ATOM = BM * 128;  // bytes of one atom column of a K/V tile
+  static constexpr uint32_t Q_ATOM = BQ * 128;   // bytes of one atom column of a Q/dO tile
+  static constexpr uint32_t DS_BYTES = BM * BQ * 2;
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_KZ = OFF_K + ATOMS * KV_ATOM;  // zero atom (D = 64 only)
+  static constexpr uint32_t OFF_V = OFF_KZ + (D == 64 ? KV_ATOM : 0);
+  static constexpr uint32_t OFF_Q = OFF_V + ATOMS * KV_ATOM;
+  static constexpr uint32_t OFF_DO = OFF_Q + STAGES * ATOMS * Q_ATOM;
+  static constexpr uint32_t OFF_DS = OFF_DO + STAGES * ATOMS * Q_ATOM;
+  static constexpr uint32_t OFF_DQ = OFF_DS + 2 * DS_BYTES;
+  static constexpr uint32_t OFF_LD = OFF_DQ + BQ * D * 4;  // per stage: lse2[BQ], D[BQ]
+  static constexpr uint32_t OFF_BAR = OFF_LD + STAGES * 2 * BQ * 4;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
+  static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
+  // tensor-memory columns
+  static constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DQ = 128, TM_DV = 256, TM_DK = 256 + D;
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);
+  static constexpr uint32_t ID_DVK = idesc_bf16(128, D, false, true);
+  static constexpr uint32_t ID_DQ = idesc_bf16(128, BQ, true, true);
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(TM_DK + D <= TM_COLS, "tensor memory budget");
+};
+
+// barrier slots
+enum : int {
+  B_KV = 0,
+  B_FULL = 1,   // + stage
+  B_EMPTY = 3,  // + stage
+  B_S = 5,
+  B_DP = 6,
+  B_P = 7,
+  B_DS = 8,
+  B_DV = 9,
+  B_DK = 10,
+  B_DQ = 11,
+  B_DQFREE = 12,
+  B_DSFREE = 13,  // + buffer
+  B_STAGED = 15,
+  B_STAGEFREE = 16,
+  B_FINAL = 17,
+  B_COUNT = 18
+};
+
+struct Params {
+  int64_t B, H, Hkv, N, M;
+  float scale;
+  int causal;
+  const float* lse;
+  const float* di;
+  const uint16_t* mask;
+  float* dq;
+  float* dk;
+  float* dv;
+  int kv_tiles;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
+  float* ld_smem = reinterpret_cast<float*>(smem + C::OFF_LD);
+
+  const int warp = (int)warp_id();
+  const int lane = (int)lane_id();
+
+  // tile coordinates: heavy (low) key tiles first so a causal grid drains evenly
+  const int64_t units = p.Hkv * p.B;
+  const int64_t j = blockIdx.x / units;
+  const int64_t rem = blockIdx.x % units;
+  const int64_t b = rem / p.Hkv, hkv = rem % p.Hkv;
+  const int64_t m0 = j * C::BM;
+  const int64_t rk2 = p.H / p.Hkv;
+  const int64_t q_tiles = (p.N + C::BQ - 1) / C::BQ;
+  int64_t qt0 = p.causal ? m0 / C::BQ : 0;
+  if (qt0 > q_tiles) qt0 = q_tiles;
+  const int64_t nqt = q_tiles - qt0;
+  const int n_it = (int)(rk2 * nqt);
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    mbar_init(bar(B_KV), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar(B_FULL + s), 32);
+      mbar_init(bar(B_EMPTY + s), 1);
+    }
+    mbar_init(bar(B_S), 1);
+    mbar_init(bar(B_DP), 1);
+    mbar_init(bar(B_P), 128);
+    mbar_init(bar(B_DS), 128);
+    mbar_init(bar(B_DV), 1);
+    mbar_init(bar(B_DK), 1);
+    mbar_init(bar(B_DQ), 1);
+    mbar_init(bar(B_DQFREE), 128);
+    mbar_init(bar(B_DSFREE + 0), 1);
+    mbar_init(bar(B_DSFREE + 1), 1);
+    mbar_init(bar(B_STAGED), 128);
+    mbar_init(bar(B_STAGEFREE), 1);
+    mbar_init(bar(B_FINAL), 1);
+    fence_mbar_init();
+  }
+  if (D == 64) {  // zero atom behind K: the upper half of the M = 128 dQ^T operand
+    uint4* z = reinterpret_cast<uint4*>(smem + C::OFF_KZ);
+    for (int i = threadIdx.x; i < (int)(C::KV_ATOM / 16); i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tmem_holder;
+  uint32_t* err = &g_err_tc;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    if (n_it > 0) {
+      if (lane == 0) {
+        prefetch_tensormap(&tmQ);
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        prefetch_tensormap(&tmO);
+        mbar_arrive_expect_tx(bar(B_KV), 2 * C::ATOMS * C::KV_ATOM);
+        const int kvrow = (int)(b * p.Hkv + hkv);
+        for (int a = 0; a < C::ATOMS; ++a) {
+          tma_load_3d(sbase + C::OFF_K + a * C::KV_ATOM, &tmK, bar(B_KV), a * 64, (int)m0, kvrow);
+          tma_load_3d(sbase + C::OFF_V + a * C::KV_ATOM, &tmV, bar(B_KV), a * 64, (int)m0, kvrow);
+        }
+      }
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % C::STAGES, u = it / C::STAGES;
+        const bool ok = mbar_wait(bar(B_EMPTY + s), (u & 1) ^ 1, abort_flag, err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const int64_t h = hkv * rk2 + it / nqt;
+        const int64_t n0 = (qt0 + it % nqt) * C::BQ;
+        const int64_t rowbase = (b * p.H + h) * p.N;
+        float* lds = ld_smem + s * 2 * C::BQ;
+        for (int jj = lane; jj < C::BQ; jj += 32) {
+          const int64_t n = n0 + jj;
+          const bool in = n < p.N;
+          lds[jj] = in ? p.lse[rowbase + n] * kLog2e : INFINITY;
+          lds[C::BQ + jj] = in ? p.di[rowbase + n] : 0.f;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_FULL + s), 2 * C::ATOMS * C::Q_ATOM);
+          const int qrow = (int)(b * p.H + h);
+          for (int a = 0; a < C::ATOMS; ++a) {
+            tma_load_3d(sbase + C::OFF_Q + (s * C::ATOMS + a) * C::Q_ATOM, &tmQ, bar(B_FULL + s), a * 64, (int)n0,
+                        qrow);
+            tma_load_4d(sbase + C::OFF_DO + (s * C::ATOMS + a) * C::Q_ATOM, &tmO, bar(B_FULL + s), a * 64, (int)h,
+                        (int)n0, (int)b);
+          }
+        } else {
+          mbar_arrive(bar(B_FULL + s));
+        }
+        ++issued;
+      }
+      // let every load this warp started land before shared memory goes away
+      if (lane == 0) {
+        mbar_drain(bar(B_KV), 0);
+        const int first = issued > C::STAGES ? issued - C::STAGES : 0;
+        for (int it = first; it < issued; ++it) mbar_drain(bar(B_FULL + it % C::STAGES), (it / C::STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_it > 0) {
+      bool ok = mbar_wait(bar(B_KV), 0, abort_flag, err);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % C::STAGES, u = it / C::STAGES;
+        const uint32_t sQ = sbase + C::OFF_Q + s * C::ATOMS * C::Q_ATOM;
+        const uint32_t sO = sbase + C::OFF_DO + s * C::ATOMS * C::Q_ATOM;
+        const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+        const uint32_t sDS = sbase + C::OFF_DS + (it & 1) * C::DS_BYTES;
+        if (!(ok = mbar_wait(bar(B_FULL + s), u & 1, abort_flag, err))) break;
+        if (it > 0 && !(ok = mbar_wait(bar(B_DV), (it - 1) & 1, abort_flag, err))) break;
+        tc_fence_after();
+        // S^T = K Q^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sK + (kk >> 2) * C::KV_ATOM + off, 16, 1024);
+          const uint64_t bq = sdesc_sw128(sQ + (kk >> 2) * C::Q_ATOM + off, 16, 1024);
+          mma_ss(tm + C::TM_S, a, bq, C::ID_S, kk > 0);
+        }
+        mma_commit(bar(B_S));
+        if (it > 0 && !(ok = mbar_wait(bar(B_DK), (it - 1) & 1, abort_flag, err))) break;
+        tc_fence_after();
+        // dP^T = V dO^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sV + (kk >> 2) * C::KV_ATOM + off, 16, 1024);
+          const uint64_t bo = sdesc_sw128(sO + (kk >> 2) * C::Q_ATOM + off, 16, 1024);
+          mma_ss(tm + C::TM_DP, a, bo, C::ID_S, kk > 0);
+        }
+        mma_commit(bar(B_DP));
+        if (!(ok = mbar_wait(bar(B_P), it & 1, abort_flag, err))) break;
+        tc_fence_after();
+        // dV += P^T dO
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk) {
+          const uint64_t bo = sdesc_sw128(sO + kk * 2048, C::Q_ATOM, 1024);
+          mma_ts(tm + C::TM_DV, tm + C::TM_S + kk * 8, bo, C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(B_DV));
+        if (!(ok = mbar_wait(bar(B_DS), it & 1, abort_flag, err))) break;
+        tc_fence_after();
+        // dK += dS^T Q
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk) {
+          const uint64_t bq = sdesc_sw128(sQ + kk * 2048, C::Q_ATOM, 1024);
+          mma_ts(tm + C::TM_DK, tm + C::TM_DP + kk * 8, bq, C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(B_DK));
+        if (it > 0 && !(ok = mbar_wait(bar(B_DQFREE), (it - 1) & 1, abort_flag, err))) break;
+        tc_fence_after();
+        // dQ^T = K^T dS^T
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk) {
+          const uint64_t a = sdesc_sw128(sK + kk * 2048, C::KV_ATOM, 1024);
+          const uint64_t bs = sdesc_sw128(sDS + kk * 2048, C::DS_BYTES, 1024);
+          mma_ss(tm + C::TM_DQ, a, bs, C::ID_DQ, kk > 0);
+        }
+        mma_commit(bar(B_DQ));
+        mma_commit(bar(B_EMPTY + s));
+        mma_commit(bar(B_DSFREE + (it & 1)));
+      }
+      // every MMA issued above must finish before tensor memory is released
+      mma_commit(bar(B_FINAL));
+      mbar_drain(bar(B_FINAL), 0);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ softmax / dS
+    const int r = (warp & 3) * 32 + lane;  // key row within the tile
+    const int64_t m = m0 + r;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float c1 = p.scale * kLog2e;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % C::STAGES, u = it / C::STAGES;
+      const int64_t n0 = (qt0 + it % nqt) * C::BQ;
+      ok = mbar_wait(bar(B_FULL + s), u & 1, abort_flag, err);
+      ok = ok && mbar_wait(bar(B_S), it & 1, abort_flag, err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const float4* lse4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ);
+      const float4* di4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ + C::BQ);
+      uint32_t ra[32], rb[32];
+      tmem_ld32(tm + lane_off + C::TM_S, ra);
+      tmem_ld32(tm + lane_off + C::TM_S + 32, rb);
+      tmem_ld_wait2(ra, rb);
+      float pv[64];
+#pragma unroll
+      for (int q4 = 0; q4 < 16; ++q4) {
+        const float4 l4 = lse4[q4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int jj = q4 * 4 + e;
+          const float sv = __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]);
+          float x = fmaf(sv, c1, -lv[e]);
+          const int64_t n = n0 + jj;
+          if (p.mask != nullptr) {
+            const float mv = (m < p.M && n < p.N) ? __half2float(__ushort_as_half(p.mask[m + p.M * n])) : 0.f;
+            x = fmaf(mv, kLog2e, x);
+          }
+          if ((p.causal && m > n) || m >= p.M) x = -INFINITY;
+          pv[jj] = ex2_approx(x);
+        }
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+      tmem_st32(tm + lane_off + C::TM_S, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_P));
+
+      ok = mbar_wait(bar(B_DP), it & 1, abort_flag, err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      tmem_ld32(tm + lane_off + C::TM_DP, ra);
+      tmem_ld32(tm + lane_off + C::TM_DP + 32, rb);
+      tmem_ld_wait2(ra, rb);
+#pragma unroll
+      for (int q4 = 0; q4 < 16; ++q4) {
+        const float4 d4 = di4[q4];
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int jj = q4 * 4 + e;
+          const float dp = __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]);
+          pv[jj] = pv[jj] * (dp - dv[e]);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+      tmem_st32(tm + lane_off + C::TM_DP, pk);
+      if (it >= 2) {
+        ok = mbar_wait(bar(B_DSFREE + (it & 1)), ((it >> 1) - 1) & 1, abort_flag, err);
+        if (!__all_sync(0xffffffffu, ok)) {
+          tmem_st_wait();
+          break;
+        }
+      }
+      // dS^T row r into the swizzled [BM x BQ] bf16 tile (16-byte chunk c of
+      // row r lives at chunk c ^ (r % 8))
+      const uint32_t rowaddr = sbase + C::OFF_DS + (it & 1) * C::DS_BYTES + r * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(rowaddr + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_DS));
+    }
+    // epilogue: dV rows of this key tile.  The tensor-memory loads are warp
+    // collectives, so every lane runs them and only the stores are per row.
+    const bool row_ok = m < p.M;
+    float* dst = p.dv + ((b * p.Hkv + hkv) * p.M + (row_ok ? m : 0)) * D;
+    if (n_it == 0) {
+      if (row_ok)
+        for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      const bool done = mbar_wait(bar(B_DV), (n_it - 1) & 1, abort_flag, err);
+      if (__all_sync(0xffffffffu, done && !*abort_flag)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ra[32];
+          tmem_ld32(tm + lane_off + C::TM_DV + c0, ra);
+          tmem_ld_wait(ra);
+          if (row_ok) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              *reinterpret_cast<float4*>(dst + c0 + c) =
+                  make_float4(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1]), __uint_as_float(ra[c + 2]),
+                              __uint_as_float(ra[c + 3]));
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain
+    const int dr = (warp & 3) * 32 + lane;  // feature row of dQ^T
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const bool leader = (warp == 6 && lane == 0);
+    float* stage = reinterpret_cast<float*>(smem + C::OFF_DQ);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int64_t h = hkv * rk2 + it / nqt;
+      const int64_t n0 = (qt0 + it % nqt) * C::BQ;
+      ok = mbar_wait(bar(B_DQ), it & 1, abort_flag, err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      __syncwarp();
+      tc_fence_after();
+      uint32_t ra[32], rb[32];
+      tmem_ld32(tm + lane_off + C::TM_DQ, ra);
+      tmem_ld32(tm + lane_off + C::TM_DQ + 32, rb);
+      tmem_ld_wait2(ra, rb);
+      tc_fence_before();
+      mbar_arrive(bar(B_DQFREE));
+      if (it > 0) {
+        ok = mbar_wait(bar(B_STAGEFREE), (it - 1) & 1, abort_flag, err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      if (dr < D) {
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj)
+          stage[jj * D + dr] = p.scale * __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(B_STAGED));
+      if (leader) {
+        if (mbar_wait(bar(B_STAGED), it & 1, abort_flag, err)) {
+          const int64_t rows = (p.N - n0) < C::BQ ? (p.N - n0) : C::BQ;
+          if (rows > 0) {
+            bulk_reduce_add_f32(p.dq + ((b * p.H + h) * p.N + n0) * D, sbase + C::OFF_DQ, (uint32_t)(rows * D * 4));
+            bulk_commit_group();
+            bulk_wait_group_read0();
+          }
+          mbar_arrive(bar(B_STAGEFREE));
+        }
+      }
+    }
+    if (leader) bulk_wait_group0();
+    __syncwarp();
+    // epilogue: dK rows of this key tile (scaled); collective loads, per-row stores
+    const int64_t m = m0 + dr;
+    const bool row_ok = m < p.M;
+    float* dst = p.dk + ((b * p.Hkv + hkv) * p.M + (row_ok ? m : 0)) * D;
+    if (n_it == 0) {
+      if (row_ok)
+        for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      const bool done = mbar_wait(bar(B_DK), (n_it - 1) & 1, abort_flag, err);
+      if (__all_sync(0xffffffffu, done && !*abort_flag)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ra[32];
+          tmem_ld32(tm + lane_off + C::TM_DK + c0, ra);
+          tmem_ld_wait(ra);
+          if (row_ok) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              *reinterpret_cast<float4*>(dst + c0 + c) =
+                  make_float4(p.scale * __uint_as_float(ra[c]), p.scale * __uint_as_float(ra[c + 1]),
+                              p.scale * __uint_as_float(ra[c + 2]), p.scale * __uint_as_float(ra[c + 3]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tm, C::TM_COLS);
+  }
+}
+
+bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+              const cuuint32_t* box) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
+  using C = Cfg<D>;
+  CUtensorMap mq, mk, mv, mo;
+  const cuuint64_t e = 2;  // bytes per bf16
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
+    const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.N * D * e};
+    const cuuint32_t box[3] = {64, (cuuint32_t)C::BQ, 1};
+    if (!make_map(&mq, pr.q, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.M, (cuuint64_t)(pr.Hkv * pr.B)};
+    const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.M * D * e};
+    const cuuint32_t box[3] = {64, (cuuint32_t)C::BM, 1};
+    if (!make_map(&mk, pr.k, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mv, pr.v, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    // d [DV,H,N,B]: rows n of one head are H*DV elements apart
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)pr.H, (cuuint64_t)pr.N, (cuuint64_t)pr.B};
+    const cuuint64_t str[3] = {D * e, (cuuint64_t)pr.H * D * e, (cuuint64_t)pr.N * pr.H * D * e};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)C::BQ, 1};
+    if (!make_map(&mo, pr.d, 4, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  Params p;
+  p.B = pr.B;
+  p.H = pr.H;
+  p.Hkv = pr.Hkv;
+  p.N = pr.N;
+  p.M = pr.M;
+  p.scale = pr.scale;
+  p.causal = pr.causal;
+  p.lse = pr.lse;
+  p.di = pr.di;
+  p.mask = pr.mask;
+  p.dq = pr.packed;
+  p.dk = pr.packed + pr.off_k / 4;
+  p.dv = pr.packed + pr.off_v / 4;
+  p.kv_tiles = (int)((pr.M + C::BM - 1) / C::BM);
+  const int64_t grid = (int64_t)p.kv_tiles * pr.Hkv * pr.B;
+  cudaError_t err = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (err != cudaSuccess) return err;
+  bwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, p);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+bool backward_tc_supported(const Problem& p) {
+  if (p.dtype != FAB_BF16 || p.DK != p.DV) return false;
+  if (p.DK != 64 && p.DK != 128) return false;
+  // TMA coordinates are 32-bit; grid.x must fit as well
+  if (p.N >= (1ll << 31) || p.M >= (1ll << 31) || p.H * p.B >= (1ll << 31)) return false;
+  return true;
+}
+
+cudaError_t launch_backward_tc(const Problem& p, cudaStream_t s) {
+  return p.DK == 128 ? launch_d<128>(p, s) : launch_d<64>(p, s);
+}
+
+uint32_t take_error_tc() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_tc, sizeof(v)) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_err_tc, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace fab

@@ -1,0 +1,226 @@
+// fab_host.cu -- the C ABI of libfab (declared in include/fab.h): argument
+// validation, packed-layout arithmetic, and the stream-ordered launches.
+// Nothing here allocates device memory or synchronises, except
+// fab_last_device_error, whose job is to synchronise.
+#include <mutex>
+
+#include "fab.h"
+#include "fab_internal.h"
+
+#define FAB_API extern "C" FAB_EXPORT
+
+namespace fab {
+
+EncodeTiledFn encode_tiled_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+namespace {
+
+constexpr int64_t kMaxWidth = 256;  // DK, DV limit of every kernel
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t pad16(int64_t bytes) { return (bytes + 15) / 16 * 16; }
+
+// The ggml_flash_attn_back constructor's shape rules (k rows as wide as q
+// rows, matching batch/head counts, H % Hkv == 0) expressed on fab_dims, plus
+// positivity and overflow guards.
+int check_dims(const fab_dims* d) {
+  if (!d) return FAB_ERR_INVALID;
+  if (d->B <= 0 || d->H <= 0 || d->Hkv <= 0 || d->N <= 0 || d->M <= 0 || d->DK <= 0 || d->DV <= 0)
+    return FAB_ERR_INVALID;
+  if (d->H % d->Hkv != 0) return FAB_ERR_INVALID;
+  const int64_t lim = kMaxElems;
+  if (d->B > lim / d->H || d->B * d->H > lim / d->N || d->B * d->H * d->N > lim / (d->DK > d->DV ? d->DK : d->DV))
+    return FAB_ERR_INVALID;
+  if (d->B > lim / d->Hkv || d->B * d->Hkv > lim / d->M ||
+      d->B * d->Hkv * d->M > lim / (d->DK > d->DV ? d->DK : d->DV))
+    return FAB_ERR_INVALID;
+  return FAB_OK;
+}
+
+void layout(const fab_dims* d, size_t* off_k, size_t* off_v, size_t* end) {
+  const int64_t elem_q = d->DK * d->N * d->H * d->B;
+  const int64_t elem_k = d->DK * d->M * d->Hkv * d->B;
+  const int64_t elem_v = d->DV * d->M * d->Hkv * d->B;
+  const int64_t ok = pad16(elem_q * 4);
+  const int64_t ov = ok + pad16(elem_k * 4);
+  *off_k = (size_t)ok;
+  *off_v = (size_t)ov;
+  *end = (size_t)(ov + pad16(elem_v * 4));
+}
+
+size_t di_bytes(const fab_dims* d) {
+  const size_t b = (size_t)(d->B * d->H * d->N) * sizeof(float);
+  return (b + 255) / 256 * 256;
+}
+
+Problem make_problem(const fab_dims* d, int dtype, float scale, int causal) {
+  Problem p{};
+  p.B = d->B;
+  p.H = d->H;
+  p.Hkv = d->Hkv;
+  p.N = d->N;
+  p.M = d->M;
+  p.DK = d->DK;
+  p.DV = d->DV;
+  p.scale = scale;
+  p.causal = causal ? 1 : 0;
+  p.dtype = dtype;
+  layout(d, &p.off_k, &p.off_v, &p.end);
+  return p;
+}
+
+bool dtype_ok(int dtype) { return dtype == FAB_F32 || dtype == FAB_BF16; }
+
+bool widths_supported(const fab_dims* d) { return d->DK <= kMaxWidth && d->DV <= kMaxWidth; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? FAB_OK : FAB_ERR_CUDA; }
+
+// Common checks of the backward entry points.  `need_*` select which pointers
+// the entry point reads.
+int check_backward(const fab_dims* dims, int dtype, const void* const* ptrs, int nptrs, const uint16_t* mask,
+                   const void* workspace, size_t workspace_bytes, const float* packed) {
+  int rc = check_dims(dims);
+  if (rc != FAB_OK) return rc;
+  if (!dtype_ok(dtype)) return FAB_ERR_INVALID;
+  for (int i = 0; i < nptrs; ++i)
+    if (!ptrs[i] || !aligned16(ptrs[i])) return FAB_ERR_INVALID;
+  if (mask && !aligned16(mask)) return FAB_ERR_INVALID;
+  if (!packed || !aligned16(packed)) return FAB_ERR_INVALID;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < di_bytes(dims)) return FAB_ERR_WORKSPACE;
+  if (!widths_supported(dims)) return FAB_ERR_UNSUPPORTED;
+  return FAB_OK;
+}
+
+}  // namespace
+}  // namespace fab
+
+using namespace fab;
+
+FAB_API int fab_version(void) { return 100; }
+
+FAB_API const char* fab_status_string(int status) {
+  switch (status) {
+    case FAB_OK:
+      return "ok";
+    case FAB_ERR_INVALID:
+      return "invalid argument (null or misaligned pointer, bad dims, H % Hkv != 0)";
+    case FAB_ERR_UNSUPPORTED:
+      return "unsupported dims or dtype for the GPU kernels";
+    case FAB_ERR_WORKSPACE:
+      return "workspace missing, misaligned or too small";
+    case FAB_ERR_CUDA:
+      return "CUDA runtime error";
+    case FAB_ERR_TIMEOUT:
+      return "a device-side wait ran out; the kernel's outputs are invalid";
+    default:
+      return "unknown status";
+  }
+}
+
+FAB_API int fab_packed_offsets(const fab_dims* dims, size_t* off_k, size_t* off_v, size_t* end) {
+  const int rc = check_dims(dims);
+  if (rc != FAB_OK) return rc;
+  size_t a, b, c;
+  layout(dims, &a, &b, &c);
+  if (off_k) *off_k = a;
+  if (off_v) *off_v = b;
+  if (end) *end = c;
+  return FAB_OK;
+}
+
+FAB_API size_t fab_packed_bytes(const fab_dims* dims) {
+  size_t end = 0;
+  if (fab_packed_offsets(dims, nullptr, nullptr, &end) != FAB_OK) return 0;
+  return end;
+}
+
+FAB_API size_t fab_backward_workspace_bytes(const fab_dims* dims, int dtype) {
+  if (check_dims(dims) != FAB_OK || !dtype_ok(dtype)) return 0;
+  return di_bytes(dims);
+}
+
+FAB_API int fab_forward_lse(const void* q, const void* k, const void* v, const uint16_t* mask, int causal,
+                            float scale, int dtype, const fab_dims* dims, void* o, float* lse, fab_stream stream) {
+  int rc = check_dims(dims);
+  if (rc != FAB_OK) return rc;
+  if (!dtype_ok(dtype)) return FAB_ERR_INVALID;
+  const void* ptrs[5] = {q, k, v, o, lse};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FAB_ERR_INVALID;
+  if (mask && !aligned16(mask)) return FAB_ERR_INVALID;
+  if (!widths_supported(dims)) return FAB_ERR_UNSUPPORTED;
+  Problem p = make_problem(dims, dtype, scale, causal);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.mask = mask;
+  return from_cuda(launch_forward_simt(p, o, lse, static_cast<cudaStream_t>(stream)));
+}
+
+FAB_API int fab_backward_preprocess(const void* d, const void* o, int dtype, const fab_dims* dims, void* workspace,
+                                    size_t workspace_bytes, float* packed_out, fab_stream stream) {
+  const void* ptrs[2] = {d, o};
+  int rc = check_backward(dims, dtype, ptrs, 2, nullptr, workspace, workspace_bytes, packed_out);
+  if (rc != FAB_OK) return rc;
+  Problem p = make_problem(dims, dtype, 1.f, 0);
+  p.d = d;
+  p.o = o;
+  p.di = static_cast<float*>(workspace);
+  p.packed = packed_out;
+  return from_cuda(launch_preprocess(p, backward_tc_supported(p), static_cast<cudaStream_t>(stream)));
+}
+
+FAB_API int fab_backward_main(const void* q, const void* k, const void* v, const void* d, const float* lse,
+                              const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims,
+                              const void* workspace, size_t workspace_bytes, float* packed_out, fab_stream stream) {
+  const void* ptrs[5] = {q, k, v, d, lse};
+  int rc = check_backward(dims, dtype, ptrs, 5, mask, workspace, workspace_bytes, packed_out);
+  if (rc != FAB_OK) return rc;
+  Problem p = make_problem(dims, dtype, scale, causal);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.d = d;
+  p.lse = lse;
+  p.mask = mask;
+  p.di = static_cast<float*>(const_cast<void*>(workspace));
+  p.packed = packed_out;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (backward_tc_supported(p)) {
+    if (!encode_tiled_fn()) return FAB_ERR_CUDA;
+    return from_cuda(launch_backward_tc(p, s));
+  }
+  return from_cuda(launch_backward_simt(p, s));
+}
+
+FAB_API int fab_backward(const void* q, const void* k, const void* v, const void* d, const void* o, const float* lse,
+                         const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims,
+                         void* workspace, size_t workspace_bytes, float* packed_out, fab_stream stream) {
+  const void* ptrs[6] = {q, k, v, d, o, lse};
+  int rc = check_backward(dims, dtype, ptrs, 6, mask, workspace, workspace_bytes, packed_out);
+  if (rc != FAB_OK) return rc;
+  rc = fab_backward_preprocess(d, o, dtype, dims, workspace, workspace_bytes, packed_out, stream);
+  if (rc != FAB_OK) return rc;
+  return fab_backward_main(q, k, v, d, lse, mask, causal, scale, dtype, dims, workspace, workspace_bytes, packed_out,
+                           stream);
+}
+
+FAB_API int fab_last_device_error(fab_stream stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FAB_ERR_CUDA;
+  const uint32_t e = take_error_tc();
+  return (e & kErrTimeout) ? FAB_ERR_TIMEOUT : FAB_OK;
+}

@@ -1,0 +1,55 @@
+// fab_internal.h -- declarations shared by the host layer and the kernel
+// translation units of libfab.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fab {
+
+// Error bits a kernel may OR into its translation unit's device error word.
+constexpr uint32_t kErrTimeout = 1u;
+
+// One validated call, in the units the kernels use.
+struct Problem {
+  int64_t B, H, Hkv, N, M, DK, DV;
+  float scale;
+  int causal;
+  int dtype;  // FAB_F32 or FAB_BF16
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* d;  // upstream gradient, [DV,H,N,B]
+  const void* o;  // forward output, [DV,H,N,B]
+  const float* lse;
+  const uint16_t* mask;  // f16 [M,N] or null
+  float* di;             // workspace: D_i, f32 [N,H,B]
+  float* packed;         // packed f32 result
+  size_t off_k, off_v, end;  // bytes
+};
+
+// fab_preprocess.cu: D_i = rowsum(dO * O) into p.di; zero the padding of the
+// packed result and, when zero_dq, the dQ slice.
+cudaError_t launch_preprocess(const Problem& p, bool zero_dq, cudaStream_t s);
+
+// fab_simt.cu: CUDA-core kernels for every dtype and width (DK, DV <= 256).
+cudaError_t launch_forward_simt(const Problem& p, void* o, float* lse, cudaStream_t s);
+cudaError_t launch_backward_simt(const Problem& p, cudaStream_t s);
+
+// fab_bwd_tc.cu: the tcgen05 tensor-core backward (bf16, DK == DV in {64, 128}).
+bool backward_tc_supported(const Problem& p);
+cudaError_t launch_backward_tc(const Problem& p, cudaStream_t s);
+
+// fab_host.cu: cuTensorMapEncodeTiled from the driver, looked up once.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// Each kernel translation unit keeps a device error word; these read and
+// clear it (host side, synchronous).
+uint32_t take_error_tc();
+
+}  // namespace fab

@@ -1,0 +1,126 @@
+// fab_preprocess.cu -- the backward's memory-bound first step.
+//
+//   D_i = dO_i . O_i  (labml "Flash Attention", "Backward pass": the per-row
+//   term sum_k P_ik dP_ik rewritten as the dot product of the output row and
+//   its gradient), for every query row (b, h, n), into a f32 [N,H,B] buffer;
+//   plus the zero fill of the packed result's padding (ggmlR packing test: the
+//   whole buffer is zeroed and padding stays 0) and, for the tensor-core path,
+//   of the dQ slice it accumulates into.
+#include <cuda_bf16.h>
+
+#include "fab.h"
+#include "fab_device.cuh"
+#include "fab_internal.h"
+
+namespace fab {
+namespace {
+
+template <typename T>
+struct Vec;  // 16-byte vector loads
+template <>
+struct Vec<float> {
+  static constexpr int kElems = 4;
+  static __device__ __forceinline__ float dot(const uint4& a, const uint4& b) {
+    return __uint_as_float(a.x) * __uint_as_float(b.x) + __uint_as_float(a.y) * __uint_as_float(b.y) +
+           __uint_as_float(a.z) * __uint_as_float(b.z) + __uint_as_float(a.w) * __uint_as_float(b.w);
+  }
+};
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+  static __device__ __forceinline__ float dot2(uint32_t a, uint32_t b) {
+    const float a0 = __uint_as_float(a << 16), a1 = __uint_as_float(a & 0xffff0000u);
+    const float b0 = __uint_as_float(b << 16), b1 = __uint_as_float(b & 0xffff0000u);
+    return a0 * b0 + a1 * b1;
+  }
+  static __device__ __forceinline__ float dot(const uint4& a, const uint4& b) {
+    return dot2(a.x, b.x) + dot2(a.y, b.y) + dot2(a.z, b.z) + dot2(a.w, b.w);
+  }
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+struct ZeroRange {
+  float* ptr;
+  int64_t n;  // floats
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ d, const T* __restrict__ o,
+                                                         float* __restrict__ di, int64_t rows, int DV, int64_t H,
+                                                         int64_t N, float4* __restrict__ zero4, int64_t zero4_n,
+                                                         ZeroRange pa, ZeroRange pb, ZeroRange pc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const bool vec = (DV % Vec<T>::kElems) == 0;
+  const int chunks = DV / Vec<T>::kElems;
+  for (int64_t r = gw; r < rows; r += warps) {
+    // r indexes rows of the [DV,H,N,B] layout: r = (b*N + n)*H + h
+    const T* dr = d + r * DV;
+    const T* orow = o + r * DV;
+    float acc = 0.f;
+    if (vec) {
+      const uint4* d4 = reinterpret_cast<const uint4*>(dr);
+      const uint4* o4 = reinterpret_cast<const uint4*>(orow);
+      for (int c = lane; c < chunks; c += 32) acc += Vec<T>::dot(__ldg(d4 + c), __ldg(o4 + c));
+    } else {
+      for (int i = lane; i < DV; i += 32) acc += to_f32(dr[i]) * to_f32(orow[i]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      const int64_t h = r % H;
+      const int64_t bn = r / H;
+      const int64_t n = bn % N, b = bn / N;
+      di[(b * H + h) * N + n] = acc;
+    }
+  }
+  const int64_t threads = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = tid; i < zero4_n; i += threads) zero4[i] = z;
+  if (tid < pa.n) pa.ptr[tid] = 0.f;
+  if (tid < pb.n) pb.ptr[tid] = 0.f;
+  if (tid < pc.n) pc.ptr[tid] = 0.f;
+}
+
+}  // namespace
+
+cudaError_t launch_preprocess(const Problem& p, bool zero_dq, cudaStream_t s) {
+  const int64_t rows = p.B * p.N * p.H;
+  const int64_t nq = p.DK * p.N * p.H * p.B, nk = p.DK * p.M * p.Hkv * p.B, nv = p.DV * p.M * p.Hkv * p.B;
+  float* base = p.packed;
+  float4* zero4 = nullptr;
+  int64_t zero4_n = 0;
+  ZeroRange pa{base + nq, (int64_t)(p.off_k / 4) - nq};
+  if (zero_dq) {  // dQ slice and its padding: [0, off_k) bytes, a multiple of 16
+    zero4 = reinterpret_cast<float4*>(base);
+    zero4_n = (int64_t)(p.off_k / 16);
+    pa.n = 0;
+  }
+  ZeroRange pb{base + p.off_k / 4 + nk, (int64_t)((p.off_v - p.off_k) / 4) - nk};
+  ZeroRange pc{base + p.off_v / 4 + nv, (int64_t)((p.end - p.off_v) / 4) - nv};
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (rows + 7) / 8;
+  const int64_t zblocks = (zero4_n + 255) / 256;
+  if (zblocks > blocks) blocks = zblocks;
+  const int64_t cap = (int64_t)sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (p.dtype == FAB_BF16) {
+    preprocess_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(p.d), static_cast<const __nv_bfloat16*>(p.o), p.di, rows, (int)p.DV, p.H,
+        p.N, zero4, zero4_n, pa, pb, pc);
+  } else {
+    preprocess_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const float*>(p.d),
+                                                              static_cast<const float*>(p.o), p.di, rows, (int)p.DV,
+                                                              p.H, p.N, zero4, zero4_n, pa, pb, pc);
+  }
+  return cudaPeekAtLastError();
+}
+
+}  // namespace fab

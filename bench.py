@@ -1,0 +1,371 @@
+"""Benchmark: attention backward TFLOP/s on GB300 through libfab's C ABI.
+
+One step = one fab_backward over the workload (D_i preprocess + the main
+gradient kernel), inputs resident in HBM, L2 flushed (256 MiB write) before
+every step.  Throughput counts 10*B*H*N*M*D flops per backward, halved for a
+causal mask.  Also reported: the main kernel's share (roofline against the
+measured dense bf16 peak), an end-to-end number with host buffers (pinned
+H2D copies of the inputs, the backward, D2H of the packed gradients), the
+forward kernel's TFLOP/s, and the fp64 CPU oracle timed on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl fab|reference]
+
+Under torchrun every rank runs the same workload on its own GPU (replicas; no
+collective on the data path) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from attention_backward_tcgen05_gb300 import inputs  # noqa: E402
+
+METRIC = "attn-backward TFLOP/s (dQ,dK,dV) and fraction of GB300 dense BF16 peak"
+DEFAULT_WORKLOAD = "gqa_causal_d128"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def backward_flops(w: inputs.Workload) -> float:
+    f = 10.0 * w.B * w.H * w.N * w.M * w.DK
+    return f / 2 if w.causal else f
+
+
+def forward_flops(w: inputs.Workload) -> float:
+    f = 4.0 * w.B * w.H * w.N * w.M * w.DK
+    return f / 2 if w.causal else f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+        self.out = os.path.join("/tmp", f"fab_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.dev)], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.out):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.out)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+
+
+def oracle_sample(w: inputs.Workload, x: dict, target_s: float = 15.0):
+    """Times the fp64 oracle on whole (batch, kv-head) units; returns (TFLOP/s, cores, sample text)."""
+    import oracle
+
+    cores = os.cpu_count() or 1
+    units_total = w.B * w.Hkv
+    # one unit per core, capped by the workload; shrink if one unit alone is slow
+    n_units = min(units_total, cores)
+    units = list(range(n_units))
+    t0 = time.perf_counter()
+    oracle.backward(x["q"], x["k"], x["v"], x["d"], x["mask"], w.causal, w.scale, units=units, threads=cores)
+    dt = time.perf_counter() - t0
+    per_unit = backward_flops(w) / units_total
+    tflops = per_unit * n_units / dt / 1e12
+    sample = (f"{n_units} of {units_total} (batch, kv-head) units of {w.name} in {dt:.1f} s; "
+              f"counted 10*B*H*N*M*D{'/2' if w.causal else ''} flops per unit")
+    return tflops, min(cores, n_units), sample, dt
+
+
+# ----------------------------------------------------------------------------- reference arm (the oracle)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    x = inputs.make(w)
+    times, vals = [], []
+    cores = os.cpu_count() or 1
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        v, c, sample, dt = oracle_sample(w, x)
+        if i >= args.warmup:
+            times.append(dt)
+            vals.append(v)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "M": w.M, "D": w.DK,
+                   "causal": w.causal, "mask": w.mask, "seed": w.seed},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": min(cores, w.B * w.Hkv),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- the fab arm
+
+
+def run_fab(args, rank, world, local):
+    from attention_backward_tcgen05_gb300 import binding
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = inputs.WORKLOADS[args.workload]
+    xc = inputs.make(w)
+    x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in xc.items()}
+    q, k, v, d, mask = x["q"], x["k"], x["v"], x["d"], x["mask"]
+    dims = binding.dims_of(q, k, v)
+    dt = binding.dtype_code(q)
+    stream = torch.cuda.current_stream()
+
+    # forward once (saved O and LSE), timed on its own
+    o, lse = binding.forward(q, k, v, mask, w.causal, w.scale)
+    fwd_ms = []
+    for i in range(3 if args.forward_steps else 0):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        binding.fab_forward_lse(q, k, v, mask, w.causal, w.scale, o, lse)
+        e1.record(stream)
+        e1.synchronize()
+        fwd_ms.append(e0.elapsed_time(e1))
+
+    ws, packed = binding.alloc_backward(dims, dt, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        binding.fab_backward_preprocess(d, o, dims, ws, packed)
+        binding.fab_backward_main(q, k, v, d, lse, mask, w.causal, w.scale, ws, packed)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    status = binding.fab_last_device_error()
+    if status != binding.FAB_OK:
+        raise RuntimeError(f"device error during warm-up: {binding.status_string(status)}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        binding.fab_backward_preprocess(d, o, dims, ws, packed)
+        ev[i][1].record(stream)
+        binding.fab_backward_main(q, k, v, d, lse, mask, w.causal, w.scale, ws, packed)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clk = clocks.stop()
+    status = binding.fab_last_device_error()
+    if status != binding.FAB_OK:
+        raise RuntimeError(f"device error in the timed region: {binding.status_string(status)}")
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    main_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world)
+    flops = backward_flops(w)
+    value = flops * world / (ms_max / 1e3) / 1e12
+
+    # end to end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {kk: vv.pin_memory() for kk, vv in xc.items() if isinstance(vv, torch.Tensor)}
+        host["o"] = o.cpu().pin_memory()
+        host["lse"] = lse.cpu().pin_memory()
+        out_host = torch.empty(packed.numel(), dtype=torch.float32).pin_memory()
+        names = [n for n in ("q", "k", "v", "d", "mask", "o", "lse") if n in host]
+        dev_buf = {n: torch.empty_like(host[n], device=dev) for n in names}
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = out_host.numel() * 4
+
+        def e2e_step():
+            for n in names:
+                dev_buf[n].copy_(host[n], non_blocking=True)
+            binding.fab_backward(dev_buf["q"], dev_buf["k"], dev_buf["v"], dev_buf["d"], dev_buf["o"],
+                                 dev_buf["lse"], dev_buf.get("mask"), w.causal, w.scale, ws, packed)
+            out_host.copy_(packed, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+        e2e = {"value": round(flops * world / (e2e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        status = binding.fab_last_device_error()
+        if status != binding.FAB_OK:
+            raise RuntimeError(f"device error in the e2e region: {binding.status_string(status)}")
+
+    peaks, peak_src = load_peaks()
+    main_mean = statistics.mean(main_ms)
+    achieved = flops / (main_mean / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": args.traffic_bytes,
+                "kernel": "bwd_tc_kernel" if (w.dtype == "bf16" and w.DK == w.DV and w.DK in (64, 128))
+                else "dq_simt_kernel+dkdv_simt_kernel",
+                "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone between L2 flushes)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, sample, _ = oracle_sample(w, xc)
+        cpu = {"value": round(v_cpu, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "M": w.M, "D": w.DK,
+                       "causal": w.causal, "mask": w.mask, "seed": w.seed, "parallelism": f"replicas x{world}",
+                       "l2": "flushed before every step (256 MiB write)"},
+            "frac_of_peak": round(value / world / peak, 4),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk,
+            "stages_ms": {"preprocess": round(statistics.mean(pre_ms), 4), "main": round(main_mean, 4)},
+            "wall_s": round(wall, 4),
+            "forward": ({"tflops": round(forward_flops(w) / (statistics.median(fwd_ms) / 1e3) / 1e12, 2),
+                         "ms": round(statistics.median(fwd_ms), 3), "kernel": "fwd_simt_kernel"}
+                        if fwd_ms else None),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["fab", "reference"], default="fab")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(inputs.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--forward-steps", type=int, default=1)
+    ap.add_argument("--traffic-bytes", type=float, default=None,
+                    help="dram read+write bytes per main-kernel launch from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_fab(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

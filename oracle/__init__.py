@@ -43,7 +43,8 @@ def _load():
         ip = ctypes.POINTER(ctypes.c_int64)
         lib.oracle_forward.argtypes = [dp, dp, dp, dp, ctypes.c_int, ctypes.c_double, ip, dp, dp, ctypes.c_int]
         lib.oracle_backward.argtypes = [dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_double, ip,
-                                        dp, dp, dp, dp, dp, dp, ip, ctypes.c_int64, ctypes.c_int]
+                                        dp, dp, dp, dp, dp, dp, ip, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_int]
         lib.oracle_di_rowdot.argtypes = [dp, dp, ip, dp]
         lib.oracle_packed_layout.argtypes = [ip, ip, ip, ip]
         lib.oracle_pack.argtypes = [ip, dp, dp, dp, dp]
@@ -103,12 +104,14 @@ def forward(q, k, v, mask=None, causal=False, scale=1.0, threads=0):
     return o, lse
 
 
-def backward(q, k, v, d, mask=None, causal=False, scale=1.0, units=None, threads=0):
+def backward(q, k, v, d, mask=None, causal=False, scale=1.0, units=None, threads=0, rows=None):
     """Analytic gradients in float64.
 
     Returns a dict with dq (B,H,N,DK), dk (B,Hkv,M,DK), dv (B,Hkv,M,DV),
     o (B,N,H,DV), lse (B,H,N) and di (B,H,N).  With ``units`` (a list of
     b*Hkv + hk indices) only those units are computed; everything else is 0.
+    With ``rows=(n_begin, n_end)`` only those query rows are visited: their
+    o/lse/di/dq rows are exact and dk/dv hold those rows' contributions only.
     """
     q, k, v, d, mask = _f64(q), _f64(k), _f64(v), _f64(d), _f64(mask)
     dims = dims_of(q, k, v)
@@ -131,7 +134,8 @@ def backward(q, k, v, d, mask=None, causal=False, scale=1.0, units=None, threads
     rc = _load().oracle_backward(
         _ptr(q), _ptr(k), _ptr(v), _ptr(d), _ptr(mask), int(bool(causal)), float(scale), da.ctypes.data_as(ip),
         _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["di"]),
-        None if u is None else u.ctypes.data_as(ip), 0 if u is None else len(u), int(threads))
+        None if u is None else u.ctypes.data_as(ip), 0 if u is None else len(u),
+        0 if rows is None else int(rows[0]), N if rows is None else int(rows[1]), int(threads))
     if rc:
         raise ValueError("oracle_backward rejected the arguments")
     return out

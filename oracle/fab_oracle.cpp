@@ -70,6 +70,9 @@ struct Problem {
   double* dq;
   double* dk;
   double* dv;
+  // query rows [n_begin, n_end) are computed (all rows by default)
+  int64_t n_begin;
+  int64_t n_end;
 };
 
 inline int64_t at_q(const Shape& s, int64_t i, int64_t n, int64_t h, int64_t b) {
@@ -189,7 +192,7 @@ void run_unit(const Problem& P, int64_t unit) {
       for (int64_t i = 0; i < s.DV; ++i) P.dv[at_v(s, i, m, hk, b)] = 0.0;
   std::vector<double> sc(s.M), p(s.M), dp(s.M);
   for (int64_t h = hk * rk2; h < (hk + 1) * rk2; ++h)
-    for (int64_t n = 0; n < s.N; ++n) one_row(P, b, h, n, sc, p, dp);
+    for (int64_t n = P.n_begin; n < P.n_end; ++n) one_row(P, b, h, n, sc, p, dp);
 }
 
 int check_shape(const int64_t* dims, Shape* s) {
@@ -242,24 +245,28 @@ int oracle_forward(const double* q, const double* k, const double* v, const doub
                    double scale, const int64_t* dims, double* out, double* lse, int n_threads) {
   Shape s;
   if (check_shape(dims, &s)) return 1;
-  Problem P{s, q, k, v, nullptr, mask, causal, scale, out, lse, nullptr, nullptr, nullptr, nullptr};
+  Problem P{s, q, k, v, nullptr, mask, causal, scale, out, lse, nullptr, nullptr, nullptr, nullptr, 0, s.N};
   run_units(P, nullptr, 0, n_threads);
   return 0;
 }
 
 // Forward and analytic backward.  Every output pointer may be null.  When
 // `units` is non-null, only those (b*Hkv + hk) units are computed; the rest of
-// each output is left as the caller initialised it.
+// each output is left as the caller initialised it.  Only query rows
+// [n_begin, n_end) are visited: their out/lse/di/dQ rows are exact, and dK/dV
+// hold the contributions of those rows alone (exact for keys that no other
+// query attends, e.g. keys >= n_begin under a causal mask when n_end = N).
 int oracle_backward(const double* q, const double* k, const double* v, const double* d, const double* mask,
                     int causal, double scale, const int64_t* dims, double* dq, double* dk, double* dv,
                     double* out, double* lse, double* di, const int64_t* units, int64_t n_units,
-                    int n_threads) {
+                    int64_t n_begin, int64_t n_end, int n_threads) {
   Shape s;
   if (check_shape(dims, &s)) return 1;
   if (!d) return 1;
   for (int64_t i = 0; units && i < n_units; ++i)
     if (units[i] < 0 || units[i] >= s.B * s.Hkv) return 1;
-  Problem P{s, q, k, v, d, mask, causal, scale, out, lse, di, dq, dk, dv};
+  if (n_begin < 0 || n_end > s.N || n_begin > n_end) return 1;
+  Problem P{s, q, k, v, d, mask, causal, scale, out, lse, di, dq, dk, dv, n_begin, n_end};
   run_units(P, units, n_units, n_threads);
   return 0;
 }

@@ -1,0 +1,143 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small cases span several key/query tiles, ragged tails, GQA, batches, causal
+and additive masks, D = 64 and 128 on the tensor-core path and odd widths /
+f32 on the CUDA-core path.  The five measured workloads run at full size in
+the launch configuration the benchmark times; where the oracle would take
+minutes, it computes a sample of (batch, key/value head) units exactly and
+the comparison covers those units.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from attention_backward_tcgen05_gb300 import binding, inputs
+from parity import TOL, check_pads_zero, compare, oracle_ref, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.lib()
+    yield
+
+
+SMALL = [
+    # name, B, H, Hkv, N, M, DK, DV, dtype, causal, mask
+    ("tc128_causal_gqa_NltM", 2, 4, 2, 200, 300, 128, 128, "bf16", True, "none"),
+    ("tc128_full_ragged", 1, 2, 2, 130, 257, 128, 128, "bf16", False, "none"),
+    ("tc128_mask_gqa", 2, 4, 1, 96, 200, 128, 128, "bf16", False, "random"),
+    ("tc128_causal_NgtM", 1, 2, 1, 300, 140, 128, 128, "bf16", True, "none"),
+    ("tc128_causal_and_mask", 1, 3, 3, 190, 190, 128, 128, "bf16", True, "random"),
+    ("tc64_causal", 2, 2, 2, 256, 256, 64, 64, "bf16", True, "none"),
+    ("tc64_mask_gqa_ragged", 1, 4, 2, 70, 130, 64, 64, "bf16", False, "random"),
+    ("tc128_single", 1, 1, 1, 1, 1, 128, 128, "bf16", False, "none"),
+    ("simt_f32_odd", 1, 2, 1, 40, 50, 16, 24, "f32", True, "none"),
+    ("simt_f32_mask", 2, 2, 2, 33, 65, 64, 64, "f32", False, "random"),
+    ("simt_bf16_odd", 1, 2, 1, 33, 47, 40, 24, "bf16", False, "random"),
+    ("simt_f32_wide", 1, 1, 1, 20, 30, 256, 200, "f32", True, "none"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_cases(case):
+    name, B, H, Hkv, N, M, DK, DV, dtype, causal, mask = case
+    w = inputs.custom(B, H, Hkv, N, M, DK, DV, dtype=dtype, causal=causal, mask=mask, seed=zlib.crc32(name.encode()) % 1000,
+                      dist="uniform" if dtype == "f32" else "normal", name=name)
+    x = inputs.make(w)
+    gpu = run_gpu(w, x)
+    ref = oracle_ref(w, x)
+    errs = compare(w, gpu, ref)
+    tol = TOL[dtype]
+    for key in ("dq", "dk", "dv", "o"):
+        assert errs[key] <= tol, (key, errs)
+    assert errs["lse"] <= 1e-3 * max(1.0, float(np.nanmax(np.abs(ref["lse"][np.isfinite(ref["lse"])]))))
+    check_pads_zero(w, gpu["packed"])
+
+
+def test_unattended_keys_and_masked_rows_exact_zero():
+    # causal with N < M leaves keys >= N unattended (a whole key tile of them);
+    # a fully masked query row must get dQ exactly 0
+    w = inputs.custom(1, 2, 1, 100, 400, 128, causal=True, mask="random", mask_p=0.05, seed=3)
+    x = inputs.make(w)
+    gpu = run_gpu(w, x)
+    assert np.all(gpu["dk"][:, :, 100:] == 0) and np.all(gpu["dv"][:, :, 100:] == 0)
+    n = x["masked_query"]
+    assert np.all(gpu["dq"][:, :, n] == 0)
+    assert np.all(gpu["o"][:, n] == 0) and np.all(np.isinf(gpu["lse"][:, :, n]))
+    ref = oracle_ref(w, x)
+    errs = compare(w, gpu, ref)
+    assert max(errs["dq"], errs["dk"], errs["dv"]) <= TOL["bf16"], errs
+
+
+def test_ones_upstream_positive_dv():
+    # d = 1: dV of an attended key is the sum of its attention weights (> 0)
+    w = inputs.custom(1, 2, 2, 128, 128, 128, seed=5)
+    x = inputs.make(w)
+    x["d"] = torch.ones_like(x["d"])
+    gpu = run_gpu(w, x)
+    assert np.all(gpu["dv"] > 0)
+
+
+def test_linearity_in_upstream_gradient():
+    w = inputs.custom(1, 2, 1, 192, 192, 128, causal=True, seed=9)
+    x = inputs.make(w)
+    a = run_gpu(w, x)
+    x2 = dict(x)
+    x2["d"] = (x["d"].float() * 2).to(x["d"].dtype)  # exact in bf16
+    b = run_gpu(w, x2)
+    for key in ("dq", "dk", "dv"):
+        np.testing.assert_allclose(b[key], 2 * a[key], rtol=1e-5, atol=1e-6)
+
+
+def test_repeat_calls_identical():
+    # the packed buffer and workspace are fully rewritten on every call
+    w = inputs.custom(2, 4, 2, 256, 256, 128, causal=True, seed=11)
+    x = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inputs.make(w).items()}
+    o, lse = binding.forward(x["q"], x["k"], x["v"], None, True, w.scale)
+    dims = binding.dims_of(x["q"], x["k"], x["v"])
+    ws, packed = binding.alloc_backward(dims, binding.FAB_BF16, x["q"].device)
+    packed.fill_(float("nan"))
+    ws.fill_(255)
+    binding.fab_backward(x["q"], x["k"], x["v"], x["d"], o, lse, None, True, w.scale, ws, packed)
+    first = packed.clone()
+    binding.fab_backward(x["q"], x["k"], x["v"], x["d"], o, lse, None, True, w.scale, ws, packed)
+    assert binding.fab_last_device_error() == binding.FAB_OK
+    assert torch.isfinite(first).all()
+    # dQ accumulation order may differ between calls; values agree to rounding
+    torch.testing.assert_close(packed, first, rtol=1e-5, atol=1e-6)
+
+
+# ----------------------------------------------------------------------------- the five workloads
+
+# (units, rows) the oracle computes exactly at full size; None = everything
+FULL_SAMPLE = {
+    "tiny_f32": (None, None),
+    "causal_d64": (None, None),
+    "gqa_causal_d128": ([0, 13, 31], None),
+    "long_seq": ([5], (16384 - 1024, 16384)),
+    "masked_nonsquare": ([0, 9, 30], None),
+}
+
+
+@pytest.mark.parametrize("name", inputs.ORDER)
+def test_workload_parity(name):
+    w = inputs.WORKLOADS[name]
+    x = inputs.make(w)
+    gpu = run_gpu(w, x)
+    units, rows = FULL_SAMPLE[name]
+    ref = oracle_ref(w, x, units=units, rows=rows)
+    errs = compare(w, gpu, ref, units=units, rows=rows)
+    tol = TOL[w.dtype]
+    for key in ("dq", "dk", "dv", "o"):
+        assert errs[key] <= tol, (name, key, errs)
+    check_pads_zero(w, gpu["packed"])
+    assert np.all(np.isfinite(gpu["packed"]))
+    if w.mask == "random":
+        n = x["masked_query"]
+        assert np.all(gpu["dq"][:, :, n] == 0), "fully masked query must get zero gradient"

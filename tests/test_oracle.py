@@ -392,3 +392,18 @@ def test_workload_inputs_shapes_and_mask():
     assert 0.05 < frac < 0.2
     y = inputs.make(w)
     assert torch.equal(x["q"], y["q"]) and torch.equal(x["mask"], y["mask"])
+
+
+def test_row_range_exact_for_late_keys_under_causal():
+    # under a causal mask only queries n >= m see key m, so visiting rows
+    # [n0, N) gives exact dK/dV for keys >= n0 and exact rows n >= n0
+    rng = np.random.default_rng(17)
+    q, k, v, d = rand_case(rng, 1, 2, 1, 12, 12, 4, 4)
+    full = oracle.backward(q, k, v, d, None, True, 0.5)
+    part = oracle.backward(q, k, v, d, None, True, 0.5, rows=(7, 12))
+    np.testing.assert_array_equal(part["dk"][:, :, 7:], full["dk"][:, :, 7:])
+    np.testing.assert_array_equal(part["dv"][:, :, 7:], full["dv"][:, :, 7:])
+    np.testing.assert_array_equal(part["dq"][:, :, 7:], full["dq"][:, :, 7:])
+    assert np.all(part["dq"][:, :, :7] == 0)
+    with pytest.raises(ValueError):
+        oracle.backward(q, k, v, d, None, True, 0.5, rows=(5, 13))
