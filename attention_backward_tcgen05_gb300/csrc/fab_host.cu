@@ -168,7 +168,12 @@ FAB_API int fab_forward_lse(const void* q, const void* k, const void* v, const u
   p.k = k;
   p.v = v;
   p.mask = mask;
-  return from_cuda(launch_forward_simt(p, o, lse, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (forward_tc_supported(p)) {
+    if (!encode_tiled_fn()) return FAB_ERR_CUDA;
+    return from_cuda(launch_forward_tc(p, o, lse, s));
+  }
+  return from_cuda(launch_forward_simt(p, o, lse, s));
 }
 
 FAB_API int fab_backward_preprocess(const void* d, const void* o, int dtype, const fab_dims* dims, void* workspace,
@@ -221,6 +226,6 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
 
 FAB_API int fab_last_device_error(fab_stream stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FAB_ERR_CUDA;
-  const uint32_t e = take_error_tc();
+  const uint32_t e = take_error_tc() | take_error_fwd();
   return (e & kErrTimeout) ? FAB_ERR_TIMEOUT : FAB_OK;
 }

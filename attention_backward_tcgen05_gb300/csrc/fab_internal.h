@@ -38,6 +38,10 @@ cudaError_t launch_preprocess(const Problem& p, bool zero_dq, cudaStream_t s);
 cudaError_t launch_forward_simt(const Problem& p, void* o, float* lse, cudaStream_t s);
 cudaError_t launch_backward_simt(const Problem& p, cudaStream_t s);
 
+// fab_fwd_tc.cu: the tcgen05 tensor-core forward with LSE (bf16, DK == DV in {64, 128}).
+bool forward_tc_supported(const Problem& p);
+cudaError_t launch_forward_tc(const Problem& p, void* o, float* lse, cudaStream_t s);
+
 // fab_bwd_tc.cu: the tcgen05 tensor-core backward (bf16, DK == DV in {64, 128}).
 bool backward_tc_supported(const Problem& p);
 cudaError_t launch_backward_tc(const Problem& p, cudaStream_t s);
@@ -51,5 +55,6 @@ EncodeTiledFn encode_tiled_fn();
 // Each kernel translation unit keeps a device error word; these read and
 // clear it (host side, synchronous).
 uint32_t take_error_tc();
+uint32_t take_error_fwd();
 
 }  // namespace fab
