@@ -27,11 +27,17 @@
 // For D = 64 the dQ^T product runs with M = 128 against a zero-filled second
 // half of A, so every product uses the 128-lane accumulator layout.
 //
-// Warp roles (320 threads): warp 0 loads tiles with TMA (and the tile's LSE
+// Warp roles (448 threads): warp 0 loads tiles with TMA (and the tile's LSE
 // and D rows); warp 1 allocates tensor memory and one lane issues every MMA;
-// warps 2-5 turn S and dP into P and dS (thread = key row); warps 6-9 drain
-// dQ^T (thread = feature row) into shared memory and issue the reductions.
-// All hand-offs are mbarriers; every wait is bounded (see fab_device.cuh).
+// warps 2-9 turn S and dP into P and dS (thread = key row; two warps share
+// each tensor-memory lane quarter and split the BQ query columns); warps
+// 10-13 drain dQ^T (thread = feature row) into shared memory and issue the
+// reductions.  All hand-offs are mbarriers; every wait is bounded (see
+// fab_device.cuh).
+//
+// Issue order per query tile i: S^T(i+1), dV(i), dK(i), dQ^T(i), dP^T(i+1).
+// S^T has two tensor-memory buffers, so the next tile's scores are computed
+// while the softmax warps turn tile i into P and dS.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,7 +51,8 @@ namespace {
 __device__ uint32_t g_err_tc;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kSoftmaxThreads = 256;
 
 template <int D>
 struct Cfg {
@@ -68,7 +75,7 @@ struct Cfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
   static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
   // tensor-memory columns
-  static constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DQ = 128, TM_DV = 256, TM_DK = 256 + D;
+  static constexpr uint32_t TM_S0 = 0, TM_DP = 64, TM_DQ = 128, TM_S1 = 192, TM_DV = 256, TM_DK = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);
   static constexpr uint32_t ID_DVK = idesc_bf16(128, D, false, true);
@@ -82,19 +89,19 @@ enum : int {
   B_KV = 0,
   B_FULL = 1,   // + stage
   B_EMPTY = 3,  // + stage
-  B_S = 5,
-  B_DP = 6,
-  B_P = 7,
-  B_DS = 8,
-  B_DV = 9,
-  B_DK = 10,
-  B_DQ = 11,
-  B_DQFREE = 12,
-  B_DSFREE = 13,  // + buffer
-  B_STAGED = 15,
-  B_STAGEFREE = 16,
-  B_FINAL = 17,
-  B_COUNT = 18
+  B_S = 5,      // + S buffer
+  B_DP = 7,
+  B_P = 8,
+  B_DS = 9,
+  B_DV = 10,
+  B_DK = 11,
+  B_DQ = 12,
+  B_DQFREE = 13,
+  B_DSFREE = 14,  // + buffer
+  B_STAGED = 16,
+  B_STAGEFREE = 17,
+  B_FINAL = 18,
+  B_COUNT = 19
 };
 
 struct Params {
@@ -148,10 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_FULL + s), 32);
       mbar_init(bar(B_EMPTY + s), 1);
     }
-    mbar_init(bar(B_S), 1);
+    mbar_init(bar(B_S + 0), 1);
+    mbar_init(bar(B_S + 1), 1);
     mbar_init(bar(B_DP), 1);
-    mbar_init(bar(B_P), 128);
-    mbar_init(bar(B_DS), 128);
+    mbar_init(bar(B_P), kSoftmaxThreads);
+    mbar_init(bar(B_DS), kSoftmaxThreads);
     mbar_init(bar(B_DV), 1);
     mbar_init(bar(B_DK), 1);
     mbar_init(bar(B_DQ), 1);
@@ -232,114 +240,136 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_it > 0) {
-      bool ok = mbar_wait(bar(B_KV), 0, abort_flag, err);
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % C::STAGES, u = it / C::STAGES;
-        const uint32_t sQ = sbase + C::OFF_Q + s * C::ATOMS * C::Q_ATOM;
-        const uint32_t sO = sbase + C::OFF_DO + s * C::ATOMS * C::Q_ATOM;
-        const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-        const uint32_t sDS = sbase + C::OFF_DS + (it & 1) * C::DS_BYTES;
-        if (!(ok = mbar_wait(bar(B_FULL + s), u & 1, abort_flag, err))) break;
-        if (it > 0 && !(ok = mbar_wait(bar(B_DV), (it - 1) & 1, abort_flag, err))) break;
-        tc_fence_after();
-        // S^T = K Q^T
+      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+      auto stage_q = [&](int it) { return sbase + C::OFF_Q + (it % C::STAGES) * C::ATOMS * C::Q_ATOM; };
+      auto stage_o = [&](int it) { return sbase + C::OFF_DO + (it % C::STAGES) * C::ATOMS * C::Q_ATOM; };
+      auto s_buf = [&](int it) { return (it & 1) ? C::TM_S1 : C::TM_S0; };
+      // S^T(it) = K Q^T into its buffer
+      auto issue_s = [&](int it) {
+        const uint32_t sQ = stage_q(it);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(sK + (kk >> 2) * C::KV_ATOM + off, 16, 1024);
-          const uint64_t bq = sdesc_sw128(sQ + (kk >> 2) * C::Q_ATOM + off, 16, 1024);
-          mma_ss(tm + C::TM_S, a, bq, C::ID_S, kk > 0);
+          mma_ss(tm + s_buf(it), sdesc_sw128(sK + (kk >> 2) * C::KV_ATOM + off, 16, 1024),
+                 sdesc_sw128(sQ + (kk >> 2) * C::Q_ATOM + off, 16, 1024), C::ID_S, kk > 0);
         }
-        mma_commit(bar(B_S));
-        if (it > 0 && !(ok = mbar_wait(bar(B_DK), (it - 1) & 1, abort_flag, err))) break;
-        tc_fence_after();
-        // dP^T = V dO^T
+        mma_commit(bar(B_S + (it & 1)));
+      };
+      // dP^T(it) = V dO^T
+      auto issue_dp = [&](int it) {
+        const uint32_t sO = stage_o(it);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(sV + (kk >> 2) * C::KV_ATOM + off, 16, 1024);
-          const uint64_t bo = sdesc_sw128(sO + (kk >> 2) * C::Q_ATOM + off, 16, 1024);
-          mma_ss(tm + C::TM_DP, a, bo, C::ID_S, kk > 0);
+          mma_ss(tm + C::TM_DP, sdesc_sw128(sV + (kk >> 2) * C::KV_ATOM + off, 16, 1024),
+                 sdesc_sw128(sO + (kk >> 2) * C::Q_ATOM + off, 16, 1024), C::ID_S, kk > 0);
         }
         mma_commit(bar(B_DP));
+      };
+      bool ok = mbar_wait(bar(B_KV), 0, abort_flag, err) && mbar_wait(bar(B_FULL), 0, abort_flag, err);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % C::STAGES;
+        if (it + 1 < n_it) {
+          // S^T(it+1) overwrites P(it-1): dV(it-1) must have read it
+          if (!(ok = mbar_wait(bar(B_FULL + (it + 1) % C::STAGES), ((it + 1) / C::STAGES) & 1, abort_flag, err)))
+            break;
+          if (it > 0 && !(ok = mbar_wait(bar(B_DV), (it - 1) & 1, abort_flag, err))) break;
+          tc_fence_after();
+          issue_s(it + 1);
+        }
         if (!(ok = mbar_wait(bar(B_P), it & 1, abort_flag, err))) break;
         tc_fence_after();
         // dV += P^T dO
+        const uint32_t sO = stage_o(it), sQ = stage_q(it);
 #pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk) {
-          const uint64_t bo = sdesc_sw128(sO + kk * 2048, C::Q_ATOM, 1024);
-          mma_ts(tm + C::TM_DV, tm + C::TM_S + kk * 8, bo, C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          mma_ts(tm + C::TM_DV, tm + s_buf(it) + kk * 8, sdesc_sw128(sO + kk * 2048, C::Q_ATOM, 1024), C::ID_DVK,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_DV));
         if (!(ok = mbar_wait(bar(B_DS), it & 1, abort_flag, err))) break;
         tc_fence_after();
         // dK += dS^T Q
 #pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk) {
-          const uint64_t bq = sdesc_sw128(sQ + kk * 2048, C::Q_ATOM, 1024);
-          mma_ts(tm + C::TM_DK, tm + C::TM_DP + kk * 8, bq, C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          mma_ts(tm + C::TM_DK, tm + C::TM_DP + kk * 8, sdesc_sw128(sQ + kk * 2048, C::Q_ATOM, 1024), C::ID_DVK,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_DK));
         if (it > 0 && !(ok = mbar_wait(bar(B_DQFREE), (it - 1) & 1, abort_flag, err))) break;
         tc_fence_after();
         // dQ^T = K^T dS^T
+        const uint32_t sDS = sbase + C::OFF_DS + (it & 1) * C::DS_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(sK + kk * 2048, C::KV_ATOM, 1024);
-          const uint64_t bs = sdesc_sw128(sDS + kk * 2048, C::DS_BYTES, 1024);
-          mma_ss(tm + C::TM_DQ, a, bs, C::ID_DQ, kk > 0);
-        }
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          mma_ss(tm + C::TM_DQ, sdesc_sw128(sK + kk * 2048, C::KV_ATOM, 1024),
+                 sdesc_sw128(sDS + kk * 2048, C::DS_BYTES, 1024), C::ID_DQ, kk > 0);
         mma_commit(bar(B_DQ));
         mma_commit(bar(B_EMPTY + s));
         mma_commit(bar(B_DSFREE + (it & 1)));
+        if (it + 1 < n_it) {
+          // dP^T(it+1) overwrites dS(it): dK(it) must have read it
+          if (!(ok = mbar_wait(bar(B_DK), it & 1, abort_flag, err))) break;
+          tc_fence_after();
+          issue_dp(it + 1);
+        }
       }
       // every MMA issued above must finish before tensor memory is released
       mma_commit(bar(B_FINAL));
       mbar_drain(bar(B_FINAL), 0);
     }
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ softmax / dS
+    // warps 2-5 take query columns 0-31 of the tile, warps 6-9 columns 32-63
+    const int hf = (warp - 2) >> 2;
     const int r = (warp & 3) * 32 + lane;  // key row within the tile
     const int64_t m = m0 + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c1 = p.scale * kLog2e;
+    // masking only where the tile needs it: keys past M, or keys past some
+    // query of the tile under the causal mask
+    const bool tail_keys = m0 + C::BM > p.M;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it % C::STAGES, u = it / C::STAGES;
-      const int64_t n0 = (qt0 + it % nqt) * C::BQ;
+      const int64_t nb = (qt0 + it % nqt) * C::BQ + hf * 32;  // first query of this thread's columns
       ok = mbar_wait(bar(B_FULL + s), u & 1, abort_flag, err);
-      ok = ok && mbar_wait(bar(B_S), it & 1, abort_flag, err);
+      ok = ok && mbar_wait(bar(B_S + (it & 1)), (it >> 1) & 1, abort_flag, err);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const float4* lse4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ);
-      const float4* di4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ + C::BQ);
-      uint32_t ra[32], rb[32];
-      tmem_ld32(tm + lane_off + C::TM_S, ra);
-      tmem_ld32(tm + lane_off + C::TM_S + 32, rb);
-      tmem_ld_wait2(ra, rb);
-      float pv[64];
+      const float4* lse4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ + hf * 32);
+      const float4* di4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ + C::BQ + hf * 32);
+      const uint32_t sb = (it & 1) ? C::TM_S1 : C::TM_S0;
+      uint32_t ra[32];
+      tmem_ld32(tm + lane_off + sb + hf * 32, ra);
+      tmem_ld_wait(ra);
+      const bool need_causal = p.causal && (m0 + C::BM - 1 > nb);
+      float pv[32];
 #pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) {
+      for (int q4 = 0; q4 < 8; ++q4) {
         const float4 l4 = lse4[q4];
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int jj = q4 * 4 + e;
-          const float sv = __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]);
-          float x = fmaf(sv, c1, -lv[e]);
-          const int64_t n = n0 + jj;
+          float x = fmaf(__uint_as_float(ra[jj]), c1, -lv[e]);
           if (p.mask != nullptr) {
+            const int64_t n = nb + jj;
             const float mv = (m < p.M && n < p.N) ? __half2float(__ushort_as_half(p.mask[m + p.M * n])) : 0.f;
             x = fmaf(mv, kLog2e, x);
           }
-          if ((p.causal && m > n) || m >= p.M) x = -INFINITY;
+          if (need_causal && m > nb + jj) x = -INFINITY;
+          if (tail_keys && m >= p.M) x = -INFINITY;
           pv[jj] = ex2_approx(x);
         }
       }
-      uint32_t pk[32];
+      uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-      tmem_st32(tm + lane_off + C::TM_S, pk);
+      for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+      tmem_st16(tm + lane_off + sb + hf * 16, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_P));
@@ -347,23 +377,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(bar(B_DP), it & 1, abort_flag, err);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      tmem_ld32(tm + lane_off + C::TM_DP, ra);
-      tmem_ld32(tm + lane_off + C::TM_DP + 32, rb);
-      tmem_ld_wait2(ra, rb);
+      tmem_ld32(tm + lane_off + C::TM_DP + hf * 32, ra);
+      tmem_ld_wait(ra);
 #pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) {
+      for (int q4 = 0; q4 < 8; ++q4) {
         const float4 d4 = di4[q4];
         const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int jj = q4 * 4 + e;
-          const float dp = __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]);
-          pv[jj] = pv[jj] * (dp - dv[e]);
+          pv[jj] = pv[jj] * (__uint_as_float(ra[jj]) - dv[e]);
         }
       }
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-      tmem_st32(tm + lane_off + C::TM_DP, pk);
+      for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+      tmem_st16(tm + lane_off + C::TM_DP + hf * 16, pk);
       if (it >= 2) {
         ok = mbar_wait(bar(B_DSFREE + (it & 1)), ((it >> 1) - 1) & 1, abort_flag, err);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -372,38 +400,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // dS^T row r into the swizzled [BM x BQ] bf16 tile (16-byte chunk c of
-      // row r lives at chunk c ^ (r % 8))
+      // row r lives at chunk c ^ (r % 8)); this thread owns chunks 4hf..4hf+3
       const uint32_t rowaddr = sbase + C::OFF_DS + (it & 1) * C::DS_BYTES + r * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_shared_v4(rowaddr + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < 4; ++c)
+        st_shared_v4(rowaddr + (((hf * 4 + c) ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                     pk[4 * c + 3]);
       fence_proxy_async_smem();
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_DS));
     }
-    // epilogue: dV rows of this key tile.  The tensor-memory loads are warp
-    // collectives, so every lane runs them and only the stores are per row.
+    // epilogue: dV rows of this key tile, half of the columns per warp.  The
+    // tensor-memory loads are warp collectives, so every lane runs them and
+    // only the stores are per row.
     const bool row_ok = m < p.M;
-    float* dst = p.dv + ((b * p.Hkv + hkv) * p.M + (row_ok ? m : 0)) * D;
+    float* dst = p.dv + ((b * p.Hkv + hkv) * p.M + (row_ok ? m : 0)) * D + hf * (D / 2);
     if (n_it == 0) {
       if (row_ok)
-        for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < D / 2; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     } else {
       const bool done = mbar_wait(bar(B_DV), (n_it - 1) & 1, abort_flag, err);
       if (__all_sync(0xffffffffu, done && !*abort_flag)) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t ra[32];
-          tmem_ld32(tm + lane_off + C::TM_DV + c0, ra);
-          tmem_ld_wait(ra);
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t rv[32];
+          tmem_ld32(tm + lane_off + C::TM_DV + hf * (D / 2) + c0, rv);
+          tmem_ld_wait(rv);
           if (row_ok) {
 #pragma unroll
             for (int c = 0; c < 32; c += 4)
               *reinterpret_cast<float4*>(dst + c0 + c) =
-                  make_float4(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1]), __uint_as_float(ra[c + 2]),
-                              __uint_as_float(ra[c + 3]));
+                  make_float4(__uint_as_float(rv[c]), __uint_as_float(rv[c + 1]), __uint_as_float(rv[c + 2]),
+                              __uint_as_float(rv[c + 3]));
           }
         }
       }
@@ -412,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ dQ drain
     const int dr = (warp & 3) * 32 + lane;  // feature row of dQ^T
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const bool leader = (warp == 6 && lane == 0);
+    const bool leader = (warp == 10 && lane == 0);
     float* stage = reinterpret_cast<float*>(smem + C::OFF_DQ);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {

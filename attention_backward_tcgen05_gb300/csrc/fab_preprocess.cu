@@ -49,28 +49,33 @@ struct ZeroRange {
 template <typename T>
 __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ d, const T* __restrict__ o,
                                                          float* __restrict__ di, int64_t rows, int DV, int64_t H,
-                                                         int64_t N, float4* __restrict__ zero4, int64_t zero4_n,
-                                                         ZeroRange pa, ZeroRange pb, ZeroRange pc) {
+                                                         int64_t N, int lpr, float4* __restrict__ zero4,
+                                                         int64_t zero4_n, ZeroRange pa, ZeroRange pb, ZeroRange pc) {
+  // `lpr` lanes (a power of two) share one row, so a warp covers 32 / lpr rows
   const int lane = threadIdx.x & 31;
+  const int sub = lane & (lpr - 1);
+  const int rpw = 32 / lpr;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const bool vec = (DV % Vec<T>::kElems) == 0;
   const int chunks = DV / Vec<T>::kElems;
-  for (int64_t r = gw; r < rows; r += warps) {
+  for (int64_t r0 = gw * rpw; r0 < rows; r0 += warps * rpw) {
     // r indexes rows of the [DV,H,N,B] layout: r = (b*N + n)*H + h
-    const T* dr = d + r * DV;
-    const T* orow = o + r * DV;
+    const int64_t r = r0 + lane / lpr;
     float acc = 0.f;
-    if (vec) {
-      const uint4* d4 = reinterpret_cast<const uint4*>(dr);
-      const uint4* o4 = reinterpret_cast<const uint4*>(orow);
-      for (int c = lane; c < chunks; c += 32) acc += Vec<T>::dot(__ldg(d4 + c), __ldg(o4 + c));
-    } else {
-      for (int i = lane; i < DV; i += 32) acc += to_f32(dr[i]) * to_f32(orow[i]);
+    if (r < rows) {
+      const T* dr = d + r * DV;
+      const T* orow = o + r * DV;
+      if (vec) {
+        const uint4* d4 = reinterpret_cast<const uint4*>(dr);
+        const uint4* o4 = reinterpret_cast<const uint4*>(orow);
+        for (int c = sub; c < chunks; c += lpr) acc += Vec<T>::dot(__ldg(d4 + c), __ldg(o4 + c));
+      } else {
+        for (int i = sub; i < DV; i += lpr) acc += to_f32(dr[i]) * to_f32(orow[i]);
+      }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
+    for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (sub == 0 && r < rows) {
       const int64_t h = r % H;
       const int64_t bn = r / H;
       const int64_t n = bn % N, b = bn / N;
@@ -105,7 +110,15 @@ cudaError_t launch_preprocess(const Problem& p, bool zero_dq, cudaStream_t s) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  int64_t blocks = (rows + 7) / 8;
+  // lanes per row: enough 16-byte chunks for every lane, at most a warp
+  const int elems = p.dtype == FAB_BF16 ? 8 : 4;
+  int lpr = 32;
+  if (p.DV % elems == 0) {
+    const int64_t chunks = p.DV / elems;
+    lpr = 1;
+    while (lpr < 32 && lpr < chunks) lpr <<= 1;
+  }
+  int64_t blocks = (rows * lpr / 32 + 7) / 8 + 1;
   const int64_t zblocks = (zero4_n + 255) / 256;
   if (zblocks > blocks) blocks = zblocks;
   const int64_t cap = (int64_t)sms * 8;
@@ -114,11 +127,11 @@ cudaError_t launch_preprocess(const Problem& p, bool zero_dq, cudaStream_t s) {
   if (p.dtype == FAB_BF16) {
     preprocess_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(p.d), static_cast<const __nv_bfloat16*>(p.o), p.di, rows, (int)p.DV, p.H,
-        p.N, zero4, zero4_n, pa, pb, pc);
+        p.N, lpr, zero4, zero4_n, pa, pb, pc);
   } else {
     preprocess_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const float*>(p.d),
                                                               static_cast<const float*>(p.o), p.di, rows, (int)p.DV,
-                                                              p.H, p.N, zero4, zero4_n, pa, pb, pc);
+                                                              p.H, p.N, lpr, zero4, zero4_n, pa, pb, pc);
   }
   return cudaPeekAtLastError();
 }

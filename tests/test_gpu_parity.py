@@ -141,3 +141,32 @@ def test_workload_parity(name):
     if w.mask == "random":
         n = x["masked_query"]
         assert np.all(gpu["dq"][:, :, n] == 0), "fully masked query must get zero gradient"
+
+
+@pytest.mark.parametrize("dtype,DV", [("bf16", 128), ("bf16", 64), ("bf16", 40), ("f32", 128), ("f32", 30)])
+def test_preprocess_di_and_zero_fill(dtype, DV):
+    import oracle
+
+    w = inputs.custom(2, 6, 3, 77, 50, 128 if DV in (64, 128) else DV, DV, dtype=dtype, seed=DV)
+    x = inputs.make(w)
+    dev = torch.device("cuda")
+    d = x["d"].to(dev)
+    o = inputs.make(inputs.custom(2, 6, 3, 77, 50, w.DK, DV, dtype=dtype, seed=DV + 1))["d"].to(dev)
+    dims = binding.make_dims(*w.dims)
+    ws, packed = binding.alloc_backward(dims, binding.dtype_code(d), dev)
+    packed.fill_(7.0)
+    binding.fab_backward_preprocess(d, o, dims, ws, packed)
+    torch.cuda.synchronize()
+    di = ws[: 2 * 6 * 77 * 4].view(torch.float32).view(2, 6, 77).double().cpu().numpy()
+    want = oracle.di_rowdot(x["d"], o.cpu())
+    np.testing.assert_allclose(di, want, rtol=1e-5, atol=1e-5)
+    p = packed.double().cpu().numpy()
+    off_k, off_v, end = (t // 4 for t in binding.fab_packed_offsets(dims))
+    nq, nk, nv = w.DK * 77 * 6 * 2, w.DK * 50 * 3 * 2, DV * 50 * 3 * 2
+    tensor_core = dtype == "bf16" and w.DK == DV and DV in (64, 128)
+    if tensor_core:  # the dQ slice is zeroed for the reductions
+        assert np.all(p[:off_k] == 0)
+    else:
+        assert np.all(p[:nq] == 7.0) and np.all(p[nq:off_k] == 0)
+    assert np.all(p[off_k:off_k + nk] == 7.0) and np.all(p[off_k + nk:off_v] == 0)
+    assert np.all(p[off_v:off_v + nv] == 7.0) and np.all(p[off_v + nv:] == 0)
