@@ -20,6 +20,8 @@
 //   S^T  = K  Q^T     [BM x BQ]  A = K (smem, K-major),  B = Q (smem, K-major)
 //   dP^T = V  dO^T    [BM x BQ]  A = V,                  B = dO
 //   P^T  = exp2(S^T * scale*log2e + mask*log2e - LSE*log2e)  -> bf16, tmem
+//          (written over the S^T columns it came from; the dV/dK products
+//          address the two 32-query halves separately)
 //   dV  += P^T dO     [BM x D]   A = P^T (tmem),         B = dO (smem, MN-major)
 //   dS^T = P^T * (dP^T - D)      -> bf16, tmem and smem
 //   dK  += dS^T Q     [BM x D]   A = dS^T (tmem),        B = Q (smem, MN-major)
@@ -244,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto stage_q = [&](int it) { return sbase + C::OFF_Q + (it % C::STAGES) * C::ATOMS * C::Q_ATOM; };
       auto stage_o = [&](int it) { return sbase + C::OFF_DO + (it % C::STAGES) * C::ATOMS * C::Q_ATOM; };
       auto s_buf = [&](int it) { return (it & 1) ? C::TM_S1 : C::TM_S0; };
+      // packed bf16 P / dS columns: queries 0-31 at +0..15, queries 32-63 at +32..47
+      auto a_col = [](int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); };
       // S^T(it) = K Q^T into its buffer
       auto issue_s = [&](int it) {
         const uint32_t sQ = stage_q(it);
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sO = stage_o(it), sQ = stage_q(it);
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ts(tm + C::TM_DV, tm + s_buf(it) + kk * 8, sdesc_sw128(sO + kk * 2048, C::Q_ATOM, 1024), C::ID_DVK,
+          mma_ts(tm + C::TM_DV, tm + s_buf(it) + a_col(kk), sdesc_sw128(sO + kk * 2048, C::Q_ATOM, 1024), C::ID_DVK,
                  (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_DV));
         if (!(ok = mbar_wait(bar(B_DS), it & 1, abort_flag, err))) break;
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dK += dS^T Q
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ts(tm + C::TM_DK, tm + C::TM_DP + kk * 8, sdesc_sw128(sQ + kk * 2048, C::Q_ATOM, 1024), C::ID_DVK,
+          mma_ts(tm + C::TM_DK, tm + C::TM_DP + a_col(kk), sdesc_sw128(sQ + kk * 2048, C::Q_ATOM, 1024), C::ID_DVK,
                  (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_DK));
         if (it > 0 && !(ok = mbar_wait(bar(B_DQFREE), (it - 1) & 1, abort_flag, err))) break;
@@ -369,7 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pk[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-      tmem_st16(tm + lane_off + sb + hf * 16, pk);
+      // packed P goes over the first 16 of this warp's own 32 S columns: the
+      // other warp of the lane quarter may still be reading its S columns
+      tmem_st16(tm + lane_off + sb + hf * 32, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_P));
@@ -391,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-      tmem_st16(tm + lane_off + C::TM_DP + hf * 16, pk);
+      tmem_st16(tm + lane_off + C::TM_DP + hf * 32, pk);
       if (it >= 2) {
         ok = mbar_wait(bar(B_DSFREE + (it & 1)), ((it >> 1) - 1) & 1, abort_flag, err);
         if (!__all_sync(0xffffffffu, ok)) {
