@@ -60,7 +60,7 @@ template <int D>
 struct Cfg {
   static constexpr int BM = 128;  // keys per CTA (tensor-memory lanes)
   static constexpr int BQ = 64;   // queries per step
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = 3;
   static constexpr int ATOMS = D / 64;  // 128-byte swizzle atoms along D
   static constexpr uint32_t KV_ATOM = BM * 128;  // bytes of one atom column of a K/V tile
   static constexpr uint32_t Q_ATOM = BQ * 128;   // bytes of one atom column of a Q/dO tile
@@ -84,27 +84,29 @@ struct Cfg {
   static constexpr uint32_t ID_DQ = idesc_bf16(128, BQ, true, true);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_DK + D <= TM_COLS, "tensor memory budget");
+  static_assert(STAGES <= 4, "barrier slots hold up to four stages");
 };
 
 // barrier slots
 enum : int {
   B_KV = 0,
-  B_FULL = 1,   // + stage
-  B_EMPTY = 3,  // + stage
-  B_S = 5,      // + S buffer
-  B_DP = 7,
-  B_P = 8,
-  B_DS = 9,
-  B_DV = 10,
-  B_DK = 11,
-  B_DQ = 12,
-  B_DQFREE = 13,
-  B_DSFREE = 14,  // + buffer
-  B_STAGED = 16,
-  B_STAGEFREE = 17,
-  B_FINAL = 18,
-  B_COUNT = 19
+  B_FULL = 1,   // + stage (up to 4)
+  B_EMPTY = 5,  // + stage (up to 4)
+  B_S = 9,      // + S buffer
+  B_DP = 11,
+  B_P = 12,
+  B_DS = 13,
+  B_DV = 14,
+  B_DK = 15,
+  B_DQ = 16,
+  B_DQFREE = 17,
+  B_DSFREE = 18,  // + buffer
+  B_STAGED = 20,
+  B_STAGEFREE = 21,
+  B_FINAL = 22,
+  B_COUNT = 23
 };
+static_assert(B_COUNT <= 32, "barrier area holds 32 slots");
 
 struct Params {
   int64_t B, H, Hkv, N, M;
@@ -212,14 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t n0 = (qt0 + it % nqt) * C::BQ;
         const int64_t rowbase = (b * p.H + h) * p.N;
         float* lds = ld_smem + s * 2 * C::BQ;
-        for (int jj = lane; jj < C::BQ; jj += 32) {
-          const int64_t n = n0 + jj;
-          const bool in = n < p.N;
-          lds[jj] = in ? p.lse[rowbase + n] * kLog2e : INFINITY;
-          lds[C::BQ + jj] = in ? p.di[rowbase + n] : 0.f;
-        }
+        // start the tile copies first; the LSE and D loads below overlap them
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(B_FULL + s), 2 * C::ATOMS * C::Q_ATOM);
+          mbar_expect_tx(bar(B_FULL + s), 2 * C::ATOMS * C::Q_ATOM);
           const int qrow = (int)(b * p.H + h);
           for (int a = 0; a < C::ATOMS; ++a) {
             tma_load_3d(sbase + C::OFF_Q + (s * C::ATOMS + a) * C::Q_ATOM, &tmQ, bar(B_FULL + s), a * 64, (int)n0,
@@ -227,9 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(sbase + C::OFF_DO + (s * C::ATOMS + a) * C::Q_ATOM, &tmO, bar(B_FULL + s), a * 64, (int)h,
                         (int)n0, (int)b);
           }
-        } else {
-          mbar_arrive(bar(B_FULL + s));
         }
+        for (int jj = lane; jj < C::BQ; jj += 32) {
+          const int64_t n = n0 + jj;
+          const bool in = n < p.N;
+          lds[jj] = in ? p.lse[rowbase + n] * kLog2e : INFINITY;
+          lds[C::BQ + jj] = in ? p.di[rowbase + n] : 0.f;
+        }
+        // one arrival per lane (count 32) publishes that lane's LSE/D stores
+        mbar_arrive(bar(B_FULL + s));
         ++issued;
       }
       // let every load this warp started land before shared memory goes away

@@ -47,6 +47,11 @@ FAB_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 
+// Raises the barrier's expected transaction bytes without arriving.
+FAB_DEV void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 FAB_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -302,13 +302,13 @@ def run_fab(args, rank, world, local):
             raise RuntimeError(f"device error in the e2e region: {binding.status_string(status)}")
 
     peaks, peak_src = load_peaks()
+    tensor_core = w.dtype == "bf16" and w.DK == w.DV and w.DK in (64, 128)
     main_mean = statistics.mean(main_ms)
     achieved = flops / (main_mean / 1e3) / 1e12
     peak = float(peaks["bf16_tflops"])
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": args.traffic_bytes,
-                "kernel": "bwd_tc_kernel" if (w.dtype == "bf16" and w.DK == w.DV and w.DK in (64, 128))
-                else "dq_simt_kernel+dkdv_simt_kernel",
+                "kernel": "bwd_tc_kernel" if tensor_core else "dq_simt_kernel+dkdv_simt_kernel",
                 "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone between L2 flushes)"}
 
     cpu = None
@@ -333,7 +333,8 @@ def run_fab(args, rank, world, local):
             "stages_ms": {"preprocess": round(statistics.mean(pre_ms), 4), "main": round(main_mean, 4)},
             "wall_s": round(wall, 4),
             "forward": ({"tflops": round(forward_flops(w) / (statistics.median(fwd_ms) / 1e3) / 1e12, 2),
-                         "ms": round(statistics.median(fwd_ms), 3), "kernel": "fwd_simt_kernel"}
+                         "ms": round(statistics.median(fwd_ms), 3),
+                         "kernel": "fwd_tc_kernel" if tensor_core else "fwd_simt_kernel"}
                         if fwd_ms else None),
         }
         print(json.dumps(line), flush=True)
