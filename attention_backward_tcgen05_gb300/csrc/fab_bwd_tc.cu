@@ -94,17 +94,17 @@ enum : int {
   B_EMPTY = 5,  // + stage (up to 4)
   B_S = 9,      // + S buffer
   B_DP = 11,
-  B_P = 12,
-  B_DS = 13,
-  B_DV = 14,
-  B_DK = 15,
-  B_DQ = 16,
-  B_DQFREE = 17,
-  B_DSFREE = 18,  // + buffer
-  B_STAGED = 20,
-  B_STAGEFREE = 21,
-  B_FINAL = 22,
-  B_COUNT = 23
+  B_P = 12,     // + S buffer: per buffer, so warps one tile ahead cannot complete a phase early
+  B_DS = 14,
+  B_DV = 15,
+  B_DK = 16,
+  B_DQ = 17,
+  B_DQFREE = 18,
+  B_DSFREE = 19,  // + buffer
+  B_STAGED = 21,
+  B_STAGEFREE = 22,
+  B_FINAL = 23,
+  B_COUNT = 24
 };
 static_assert(B_COUNT <= 32, "barrier area holds 32 slots");
 
@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_S + 0), 1);
     mbar_init(bar(B_S + 1), 1);
     mbar_init(bar(B_DP), 1);
-    mbar_init(bar(B_P), kSoftmaxThreads);
+    mbar_init(bar(B_P + 0), kSoftmaxThreads);
+    mbar_init(bar(B_P + 1), kSoftmaxThreads);
     mbar_init(bar(B_DS), kSoftmaxThreads);
     mbar_init(bar(B_DV), 1);
     mbar_init(bar(B_DK), 1);
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(it + 1);
         }
-        if (!(ok = mbar_wait(bar(B_P), it & 1, abort_flag, err))) break;
+        if (!(ok = mbar_wait(bar(B_P + (it & 1)), (it >> 1) & 1, abort_flag, err))) break;
         tc_fence_after();
         // dV += P^T dO
         const uint32_t sO = stage_o(it), sQ = stage_q(it);
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st16(tm + lane_off + sb + hf * 32, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_P));
+      mbar_arrive(bar(B_P + (it & 1)));
 
       ok = mbar_wait(bar(B_DP), it & 1, abort_flag, err);
       if (!__all_sync(0xffffffffu, ok)) break;
