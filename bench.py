@@ -265,38 +265,80 @@ def run_fab(args, rank, world, local):
     flops = backward_flops(w)
     value = flops * world / (ms_max / 1e3) / 1e12
 
-    # end to end through the public call with host buffers
+    # end to end through the public call with host buffers: every step copies
+    # its inputs from pinned host memory, runs fab_backward and reads the packed
+    # gradients back.  "e2e" overlaps steps (H2D of step i+1 and D2H of step
+    # i-1 run on their own streams while step i computes, two buffer sets);
+    # "serial" runs the three phases of each step back to back on one stream.
     e2e = None
     if not args.no_e2e:
         host = {kk: vv.pin_memory() for kk, vv in xc.items() if isinstance(vv, torch.Tensor)}
         host["o"] = o.cpu().pin_memory()
         host["lse"] = lse.cpu().pin_memory()
-        out_host = torch.empty(packed.numel(), dtype=torch.float32).pin_memory()
         names = [n for n in ("q", "k", "v", "d", "mask", "o", "lse") if n in host]
-        dev_buf = {n: torch.empty_like(host[n], device=dev) for n in names}
         h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-        d2h = out_host.numel() * 4
+        d2h = packed.numel() * 4
+        sets = []
+        for _ in range(2):
+            bufs = {n: torch.empty_like(host[n], device=dev) for n in names}
+            wsb, pkb = binding.alloc_backward(dims, dt, dev)
+            sets.append((bufs, wsb, pkb, torch.empty(packed.numel(), dtype=torch.float32).pin_memory()))
+        s_h2d, s_cmp, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-        def e2e_step():
-            for n in names:
-                dev_buf[n].copy_(host[n], non_blocking=True)
-            binding.fab_backward(dev_buf["q"], dev_buf["k"], dev_buf["v"], dev_buf["d"], dev_buf["o"],
-                                 dev_buf["lse"], dev_buf.get("mask"), w.causal, w.scale, ws, packed)
-            out_host.copy_(packed, non_blocking=True)
+        def run_pipelined(nsteps):
+            ev_in = [torch.cuda.Event() for _ in range(2)]
+            ev_cmp = [torch.cuda.Event() for _ in range(2)]
+            ev_out = [torch.cuda.Event() for _ in range(2)]
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(s_h2d)
+            for i in range(nsteps):
+                bufs, wsb, pkb, outh = sets[i % 2]
+                if i >= 2:
+                    s_h2d.wait_event(ev_cmp[i % 2])  # inputs of step i-2 consumed
+                with torch.cuda.stream(s_h2d):
+                    for n in names:
+                        bufs[n].copy_(host[n], non_blocking=True)
+                    ev_in[i % 2].record(s_h2d)
+                s_cmp.wait_event(ev_in[i % 2])
+                if i >= 2:
+                    s_cmp.wait_event(ev_out[i % 2])  # packed of step i-2 read back
+                binding.fab_backward(bufs["q"], bufs["k"], bufs["v"], bufs["d"], bufs["o"], bufs["lse"],
+                                     bufs.get("mask"), w.causal, w.scale, wsb, pkb, stream=s_cmp)
+                ev_cmp[i % 2].record(s_cmp)
+                s_d2h.wait_event(ev_cmp[i % 2])
+                with torch.cuda.stream(s_d2h):
+                    outh.copy_(pkb, non_blocking=True)
+                    ev_out[i % 2].record(s_d2h)
+            s_d2h.wait_event(ev_out[(nsteps - 1) % 2])
+            t1.record(s_d2h)
+            t1.synchronize()
+            return t0.elapsed_time(t1) / nsteps
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        def run_serial(nsteps):
+            bufs, wsb, pkb, outh = sets[0]
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(nsteps):
+                for n in names:
+                    bufs[n].copy_(host[n], non_blocking=True)
+                binding.fab_backward(bufs["q"], bufs["k"], bufs["v"], bufs["d"], bufs["o"], bufs["lse"],
+                                     bufs.get("mask"), w.causal, w.scale, wsb, pkb)
+                outh.copy_(pkb, non_blocking=True)
+            t1.record(stream)
+            t1.synchronize()
+            return t0.elapsed_time(t1) / nsteps
+
+        run_pipelined(max(2, args.warmup))
+        run_serial(max(1, args.warmup))
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        e1.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
-        e2e = {"value": round(flops * world / (e2e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
-               "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        pipe_ms = max_over_ranks(run_pipelined(args.steps), world)
+        barrier(world)
+        ser_ms = max_over_ranks(run_serial(args.steps), world)
+        e2e = {"value": round(flops * world / (pipe_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(pipe_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "mode": "two buffer sets, H2D / backward / D2H on three streams, steps overlapped",
+               "serial": {"value": round(flops * world / (ser_ms / 1e3) / 1e12, 3), "ms_per_step": round(ser_ms, 3)}}
         status = binding.fab_last_device_error()
         if status != binding.FAB_OK:
             raise RuntimeError(f"device error in the e2e region: {binding.status_string(status)}")
