@@ -27,7 +27,8 @@ FAB_F32, FAB_BF16 = 0, 1
 
 EXPORTS = ("fab_version", "fab_status_string", "fab_packed_offsets", "fab_packed_bytes",
            "fab_backward_workspace_bytes", "fab_forward_lse", "fab_backward", "fab_backward_preprocess",
-           "fab_backward_main", "fab_last_device_error")
+           "fab_backward_main", "fab_backward_noalloc", "fab_last_device_error")
+NOALLOC_MAX_ROWS = 1048576  # FAB_NOALLOC_MAX_ROWS
 
 
 class fab_dims(ctypes.Structure):
@@ -69,6 +70,7 @@ def lib():
                     "fab_backward": ([vp, vp, vp, vp, vp, vp, vp, i32, f32, i32, dp, vp, sz, vp, vp], i32),
                     "fab_backward_preprocess": ([vp, vp, i32, dp, vp, sz, vp, vp], i32),
                     "fab_backward_main": ([vp, vp, vp, vp, vp, vp, i32, f32, i32, dp, vp, sz, vp, vp], i32),
+                    "fab_backward_noalloc": ([vp, vp, vp, vp, vp, vp, vp, i32, f32, i32, dp, vp, vp], i32),
                     "fab_last_device_error": ([vp], i32),
                 }
                 for name, (args, res) in sig.items():
@@ -198,6 +200,20 @@ def fab_backward_main(q, k, v, d, lse, mask, causal, scale, workspace, packed_ou
             workspace.numel() * workspace.element_size(),
             _dev(packed_out, "packed_out", torch.float32, (fab_packed_bytes(dims) // 4,)), _stream(stream))
     _check(lib().fab_backward_main(*args), "fab_backward_main")
+
+
+def fab_backward_noalloc(q, k, v, d, o, lse, mask, causal, scale, packed_out, stream=None):
+    """fab_backward without a workspace: for callers that cannot allocate
+    device memory.  The scratch is a fixed array inside libfab (B*H*N up to
+    NOALLOC_MAX_ROWS); calls that may overlap on the GPU must be ordered."""
+    dims = dims_of(q, k, v)
+    t = dtype_code(q)
+    oshape = (dims.B, dims.N, dims.H, dims.DV)
+    args = (_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), _dev(d, "d", q.dtype, oshape),
+            _dev(o, "o", q.dtype, oshape), _dev(lse, "lse", torch.float32, (dims.B, dims.H, dims.N)),
+            _mask(mask, dims), int(bool(causal)), float(scale), t, ctypes.byref(dims),
+            _dev(packed_out, "packed_out", torch.float32, (fab_packed_bytes(dims) // 4,)), _stream(stream))
+    _check(lib().fab_backward_noalloc(*args), "fab_backward_noalloc")
 
 
 def fab_last_device_error(stream=None) -> int:

@@ -144,6 +144,27 @@ FAB_EXPORT int fab_backward_main(const void* q, const void* k, const void* v, co
                       const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims,
                       const void* workspace, size_t workspace_bytes, float* packed_out, fab_stream stream);
 
+/* Largest B*H*N that fab_backward_noalloc accepts (query rows times heads
+ * times batches): its fixed scratch holds one float per such row. */
+#define FAB_NOALLOC_MAX_ROWS 1048576
+
+/* fab_backward for callers that cannot allocate device memory, for example
+ * code whose device memory belongs to another allocator, or code that must not
+ * call cudaMalloc (which can synchronise the device) on its path.  The pages
+ * have no counterpart; the operation and every argument are those of
+ * fab_backward minus the workspace.  The workspace lives instead in a fixed
+ * device array inside the library: FAB_NOALLOC_MAX_ROWS floats (4 MiB), held
+ * on every GPU that loads the library until the process exits.  Returns
+ * FAB_ERR_WORKSPACE when B*H*N exceeds FAB_NOALLOC_MAX_ROWS; allocates and
+ * frees nothing.  The first call on a device looks up the array's device
+ * address with that device current; make that first call before any stream
+ * capture.  Calls on one device share the array, so two calls that may run
+ * at the same time on the GPU (on unordered streams) race; order them.  No
+ * part of the array needs clearing between calls. */
+FAB_EXPORT int fab_backward_noalloc(const void* q, const void* k, const void* v, const void* d, const void* o,
+                                    const float* lse, const uint16_t* mask, int causal, float scale, int dtype,
+                                    const fab_dims* dims, float* packed_out, fab_stream stream);
+
 /* Synchronises `stream`, then returns and clears the device-side error word
  * of the current device: FAB_OK, FAB_ERR_TIMEOUT (a bounded wait inside a
  * kernel ran out; that kernel's outputs are invalid) or FAB_ERR_CUDA. */
