@@ -23,8 +23,8 @@
 //          (written over the S^T columns it came from; the dV/dK products
 //          address the two 32-query halves separately)
 //   dV  += P^T dO     [BM x D]   A = P^T (tmem),         B = dO (smem, MN-major)
-//   dS^T = P^T * (dP^T - D)      -> bf16, tmem and smem
-//   dK  += dS^T Q     [BM x D]   A = dS^T (tmem),        B = Q (smem, MN-major)
+//   dS^T = P^T * (dP^T - D)      -> bf16, smem (128-byte swizzled, key rows)
+//   dK  += dS^T Q     [BM x D]   A = dS^T (smem, K-major), B = Q (smem, MN-major)
 //   dQ^T = K^T dS^T   [D x BQ]   A = K (smem, MN-major), B = dS^T (smem, MN-major)
 // For D = 64 the dQ^T product runs with M = 128 against a zero-filled second
 // half of A, so every product uses the 128-lane accumulator layout.
@@ -37,9 +37,10 @@
 // reductions.  All hand-offs are mbarriers; every wait is bounded (see
 // fab_device.cuh).
 //
-// Issue order per query tile i: S^T(i+1), dV(i), dK(i), dQ^T(i), dP^T(i+1).
-// S^T has two tensor-memory buffers, so the next tile's scores are computed
-// while the softmax warps turn tile i into P and dS.
+// Issue order per query tile i: dV(i) | dP^T(i+1), dK(i), dQ^T(i) | S^T(i+2).
+// S^T has two tensor-memory buffers, so scores run two tiles ahead of the
+// softmax warps; dP^T(i+1) is issued as soon as the softmax warps have read
+// dP^T(i) (dS lives in shared memory, so no product reads the dP^T columns).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -274,43 +275,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar(B_DP));
       };
+      // prologue: S^T(0), dP^T(0), S^T(1)
       bool ok = mbar_wait(bar(B_KV), 0, abort_flag, err) && mbar_wait(bar(B_FULL), 0, abort_flag, err);
       if (ok) {
         tc_fence_after();
         issue_s(0);
         issue_dp(0);
+        if (n_it > 1 && (ok = mbar_wait(bar(B_FULL + 1), 0, abort_flag, err))) {
+          tc_fence_after();
+          issue_s(1);
+        }
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it % C::STAGES;
-        if (it + 1 < n_it) {
-          // S^T(it+1) overwrites P(it-1): dV(it-1) must have read it
-          if (!(ok = mbar_wait(bar(B_FULL + (it + 1) % C::STAGES), ((it + 1) / C::STAGES) & 1, abort_flag, err)))
-            break;
-          if (it > 0 && !(ok = mbar_wait(bar(B_DV), (it - 1) & 1, abort_flag, err))) break;
-          tc_fence_after();
-          issue_s(it + 1);
-        }
+        const uint32_t sO = stage_o(it), sQ = stage_q(it);
+        const uint32_t sDS = sbase + C::OFF_DS + (it & 1) * C::DS_BYTES;
+        // dV += P^T dO, P^T from this tile's score buffer
         if (!(ok = mbar_wait(bar(B_P + (it & 1)), (it >> 1) & 1, abort_flag, err))) break;
         tc_fence_after();
-        // dV += P^T dO
-        const uint32_t sO = stage_o(it), sQ = stage_q(it);
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
           mma_ts(tm + C::TM_DV, tm + s_buf(it) + a_col(kk), sdesc_sw128(sO + kk * 2048, C::Q_ATOM, 1024), C::ID_DVK,
                  (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(B_DV));
+        // dS^T(it) is in shared memory and dP^T(it) has been read: the next
+        // tile's dP^T goes first so its dS work overlaps dK(it) and dQ^T(it)
         if (!(ok = mbar_wait(bar(B_DS), it & 1, abort_flag, err))) break;
         tc_fence_after();
-        // dK += dS^T Q
+        if (it + 1 < n_it) issue_dp(it + 1);
+        // dK += dS^T Q, both from shared memory (dS^T K-major, Q MN-major)
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ts(tm + C::TM_DK, tm + C::TM_DP + a_col(kk), sdesc_sw128(sQ + kk * 2048, C::Q_ATOM, 1024), C::ID_DVK,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(B_DK));
+          mma_ss(tm + C::TM_DK, sdesc_sw128(sDS + kk * 32, 16, 1024), sdesc_sw128(sQ + kk * 2048, C::Q_ATOM, 1024),
+                 C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u);
         if (it > 0 && !(ok = mbar_wait(bar(B_DQFREE), (it - 1) & 1, abort_flag, err))) break;
         tc_fence_after();
         // dQ^T = K^T dS^T
-        const uint32_t sDS = sbase + C::OFF_DS + (it & 1) * C::DS_BYTES;
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
           mma_ss(tm + C::TM_DQ, sdesc_sw128(sK + kk * 2048, C::KV_ATOM, 1024),
@@ -318,11 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(B_DQ));
         mma_commit(bar(B_EMPTY + s));
         mma_commit(bar(B_DSFREE + (it & 1)));
-        if (it + 1 < n_it) {
-          // dP^T(it+1) overwrites dS(it): dK(it) must have read it
-          if (!(ok = mbar_wait(bar(B_DK), it & 1, abort_flag, err))) break;
+        if (it + 2 < n_it) {
+          // S^T(it+2) overwrites P(it) in the same buffer: dV(it) must have read it
+          if (!(ok = mbar_wait(bar(B_FULL + (it + 2) % C::STAGES), ((it + 2) / C::STAGES) & 1, abort_flag, err)))
+            break;
+          if (!(ok = mbar_wait(bar(B_DV), it & 1, abort_flag, err))) break;
           tc_fence_after();
-          issue_dp(it + 1);
+          issue_s(it + 2);
         }
       }
       // every MMA issued above must finish before tensor memory is released
@@ -401,13 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-      tmem_st16(tm + lane_off + C::TM_DP + hf * 32, pk);
       if (it >= 2) {
         ok = mbar_wait(bar(B_DSFREE + (it & 1)), ((it >> 1) - 1) & 1, abort_flag, err);
-        if (!__all_sync(0xffffffffu, ok)) {
-          tmem_st_wait();
-          break;
-        }
+        if (!__all_sync(0xffffffffu, ok)) break;
       }
       // dS^T row r into the swizzled [BM x BQ] bf16 tile (16-byte chunk c of
       // row r lives at chunk c ^ (r % 8)); this thread owns chunks 4hf..4hf+3
@@ -417,8 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_shared_v4(rowaddr + (((hf * 4 + c) ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
                      pk[4 * c + 3]);
       fence_proxy_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
+      tc_fence_before();  // the dP^T reads above are done before dP^T(it+1) may overwrite them
       mbar_arrive(bar(B_DS));
     }
     // epilogue: dV rows of this key tile, half of the columns per warp.  The
@@ -430,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row_ok)
         for (int c = 0; c < D / 2; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     } else {
-      const bool done = mbar_wait(bar(B_DV), (n_it - 1) & 1, abort_flag, err);
+      const bool done = mbar_wait(bar(B_FINAL), 0, abort_flag, err);
       if (__all_sync(0xffffffffu, done && !*abort_flag)) {
         tc_fence_after();
 #pragma unroll 1
@@ -501,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row_ok)
         for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     } else {
-      const bool done = mbar_wait(bar(B_DK), (n_it - 1) & 1, abort_flag, err);
+      const bool done = mbar_wait(bar(B_FINAL), 0, abort_flag, err);
       if (__all_sync(0xffffffffu, done && !*abort_flag)) {
         tc_fence_after();
 #pragma unroll 1
