@@ -12,8 +12,9 @@
 // batch).  The key/value tile stays in shared memory; the CTA walks every
 // query head of the GQA group and every query tile of BQ = 64 queries
 // (skipping tiles a top-left causal mask empties), so dK and dV of the group
-// accumulate in tensor memory without atomics.  dQ tiles are reduced into the
-// packed dQ slice (zeroed beforehand) with bulk async f32 reductions.
+// accumulate in tensor memory without atomics.  dQ tiles are added into the
+// packed dQ slice (zeroed beforehand) with fire-and-forget f32 reductions
+// (red.global.add) straight from registers.
 //
 // Per query tile, all in the transposed ("key rows") orientation so that one
 // thread owns one key row of every tensor-memory tile:
@@ -33,8 +34,9 @@
 // and D rows); warp 1 allocates tensor memory and one lane issues every MMA;
 // warps 2-9 turn S and dP into P and dS (thread = key row; two warps share
 // each tensor-memory lane quarter and split the BQ query columns); warps
-// 10-13 drain dQ^T (thread = feature row) into shared memory and issue the
-// reductions.  All hand-offs are mbarriers; every wait is bounded (see
+// 10-13 drain dQ^T (thread = feature row) and add it into the packed dQ slice
+// (consecutive lanes hit consecutive features, 128 contiguous bytes per warp
+// and query).  All hand-offs are mbarriers; every wait is bounded (see
 // fab_device.cuh).
 //
 // Issue order per query tile i: dV(i) | dP^T(i+1), dK(i), dQ^T(i) | S^T(i+2).
@@ -61,7 +63,7 @@ template <int D>
 struct Cfg {
   static constexpr int BM = 128;  // keys per CTA (tensor-memory lanes)
   static constexpr int BQ = 64;   // queries per step
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = 4;
   static constexpr int ATOMS = D / 64;  // 128-byte swizzle atoms along D
   static constexpr uint32_t KV_ATOM = BM * 128;  // bytes of one atom column of a K/V tile
   static constexpr uint32_t Q_ATOM = BQ * 128;   // bytes of one atom column of a Q/dO tile
@@ -72,11 +74,10 @@ struct Cfg {
   static constexpr uint32_t OFF_Q = OFF_V + ATOMS * KV_ATOM;
   static constexpr uint32_t OFF_DO = OFF_Q + STAGES * ATOMS * Q_ATOM;
   static constexpr uint32_t OFF_DS = OFF_DO + STAGES * ATOMS * Q_ATOM;
-  static constexpr uint32_t OFF_DQ = OFF_DS + 2 * DS_BYTES;
-  static constexpr uint32_t OFF_LD = OFF_DQ + BQ * D * 4;  // per stage: lse2[BQ], D[BQ]
+  static constexpr uint32_t OFF_LD = OFF_DS + 2 * DS_BYTES;  // per stage: lse2[BQ], D[BQ]
   static constexpr uint32_t OFF_BAR = OFF_LD + STAGES * 2 * BQ * 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
-  static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
+  static constexpr uint32_t SMEM = OFF_MISC + 64;
   // tensor-memory columns
   static constexpr uint32_t TM_S0 = 0, TM_DP = 64, TM_DQ = 128, TM_S1 = 192, TM_DV = 256, TM_DK = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
@@ -102,10 +103,8 @@ enum : int {
   B_DQ = 17,
   B_DQFREE = 18,
   B_DSFREE = 19,  // + buffer
-  B_STAGED = 21,
-  B_STAGEFREE = 22,
-  B_FINAL = 23,
-  B_COUNT = 24
+  B_FINAL = 21,
+  B_COUNT = 22
 };
 static_assert(B_COUNT <= 32, "barrier area holds 32 slots");
 
@@ -129,7 +128,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem_raw) & 1023u) {  // swizzled tiles need a 1024-byte-aligned base
+    if (threadIdx.x == 0) atomicOr(&g_err_tc, kErrSmemAlign);
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -172,8 +175,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DQFREE), 128);
     mbar_init(bar(B_DSFREE + 0), 1);
     mbar_init(bar(B_DSFREE + 1), 1);
-    mbar_init(bar(B_STAGED), 128);
-    mbar_init(bar(B_STAGEFREE), 1);
     mbar_init(bar(B_FINAL), 1);
     fence_mbar_init();
   }
@@ -246,89 +247,99 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_it > 0) {
-      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-      auto stage_q = [&](int it) { return sbase + C::OFF_Q + (it % C::STAGES) * C::ATOMS * C::Q_ATOM; };
-      auto stage_o = [&](int it) { return sbase + C::OFF_DO + (it % C::STAGES) * C::ATOMS * C::Q_ATOM; };
+    // the whole warp runs this loop (descriptors stay warp-uniform); lane 0
+    // issues the MMAs and commits
+    if (n_it > 0) {
+      const uint32_t issue = lane == 0 ? 1u : 0u;
+      auto wall = [&](int i, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, err));
+      };
+      // Descriptors are built once; a K step only moves the start address,
+      // whose 14-bit field (address >> 4, all addresses < 232 KB) never carries
+      // into the neighbouring fields, so a step is one add.
+      auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
+      const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);               // K, K-major
+      const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);               // V, K-major
+      const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::KV_ATOM, 1024);       // K, MN-major (dQ^T A)
+      const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);               // stage 0 Q, K-major
+      const uint64_t dQ_mn = sdesc_sw128(sbase + C::OFF_Q, C::Q_ATOM, 1024);        // stage 0 Q, MN-major
+      const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+      const uint64_t dO_mn = sdesc_sw128(sbase + C::OFF_DO, C::Q_ATOM, 1024);
+      const uint64_t dS_km = sdesc_sw128(sbase + C::OFF_DS, 16, 1024);              // dS^T buffer 0, K-major
+      const uint64_t dS_mn = sdesc_sw128(sbase + C::OFF_DS, C::DS_BYTES, 1024);     // dS^T buffer 0, MN-major
+      auto stage_off = [](int it) { return (uint32_t)((it % C::STAGES) * C::ATOMS * C::Q_ATOM); };
       auto s_buf = [&](int it) { return (it & 1) ? C::TM_S1 : C::TM_S0; };
-      // packed bf16 P / dS columns: queries 0-31 at +0..15, queries 32-63 at +32..47
+      // packed bf16 P columns: queries 0-31 at +0..15, queries 32-63 at +32..47
       auto a_col = [](int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); };
+      // byte offset of K step kk inside a K-major tile whose atom columns are `atom` bytes apart
+      auto kstep = [](int kk, uint32_t atom) { return (uint32_t)((kk >> 2) * atom + (kk & 3) * 32); };
       // S^T(it) = K Q^T into its buffer
       auto issue_s = [&](int it) {
-        const uint32_t sQ = stage_q(it);
+        const uint64_t q = adv(dQ_km, stage_off(it));
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          mma_ss(tm + s_buf(it), sdesc_sw128(sK + (kk >> 2) * C::KV_ATOM + off, 16, 1024),
-                 sdesc_sw128(sQ + (kk >> 2) * C::Q_ATOM + off, 16, 1024), C::ID_S, kk > 0);
-        }
-        mma_commit(bar(B_S + (it & 1)));
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tm + s_buf(it), adv(dK_km, kstep(kk, C::KV_ATOM)), adv(q, kstep(kk, C::Q_ATOM)), C::ID_S, kk > 0, issue);
+        mma_commit(bar(B_S + (it & 1)), issue);
       };
       // dP^T(it) = V dO^T
       auto issue_dp = [&](int it) {
-        const uint32_t sO = stage_o(it);
+        const uint64_t o = adv(dO_km, stage_off(it));
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          mma_ss(tm + C::TM_DP, sdesc_sw128(sV + (kk >> 2) * C::KV_ATOM + off, 16, 1024),
-                 sdesc_sw128(sO + (kk >> 2) * C::Q_ATOM + off, 16, 1024), C::ID_S, kk > 0);
-        }
-        mma_commit(bar(B_DP));
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tm + C::TM_DP, adv(dV_km, kstep(kk, C::KV_ATOM)), adv(o, kstep(kk, C::Q_ATOM)), C::ID_S, kk > 0, issue);
+        mma_commit(bar(B_DP), issue);
       };
       // prologue: S^T(0), dP^T(0), S^T(1)
-      bool ok = mbar_wait(bar(B_KV), 0, abort_flag, err) && mbar_wait(bar(B_FULL), 0, abort_flag, err);
+      bool ok = wall(B_KV, 0) && wall(B_FULL, 0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
         issue_dp(0);
-        if (n_it > 1 && (ok = mbar_wait(bar(B_FULL + 1), 0, abort_flag, err))) {
+        if (n_it > 1 && (ok = wall(B_FULL + 1, 0))) {
           tc_fence_after();
           issue_s(1);
         }
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it % C::STAGES;
-        const uint32_t sO = stage_o(it), sQ = stage_q(it);
-        const uint32_t sDS = sbase + C::OFF_DS + (it & 1) * C::DS_BYTES;
+        const uint64_t o_mn = adv(dO_mn, stage_off(it)), q_mn = adv(dQ_mn, stage_off(it));
+        const uint64_t ds_km = adv(dS_km, (it & 1) * C::DS_BYTES), ds_mn = adv(dS_mn, (it & 1) * C::DS_BYTES);
         // dV += P^T dO, P^T from this tile's score buffer
-        if (!(ok = mbar_wait(bar(B_P + (it & 1)), (it >> 1) & 1, abort_flag, err))) break;
+        if (!(ok = wall(B_P + (it & 1), (it >> 1) & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ts(tm + C::TM_DV, tm + s_buf(it) + a_col(kk), sdesc_sw128(sO + kk * 2048, C::Q_ATOM, 1024), C::ID_DVK,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(B_DV));
+          mma_ts(tm + C::TM_DV, tm + s_buf(it) + a_col(kk), adv(o_mn, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u, issue);
+        mma_commit(bar(B_DV), issue);
         // dS^T(it) is in shared memory and dP^T(it) has been read: the next
         // tile's dP^T goes first so its dS work overlaps dK(it) and dQ^T(it)
-        if (!(ok = mbar_wait(bar(B_DS), it & 1, abort_flag, err))) break;
+        if (!(ok = wall(B_DS, it & 1))) break;
         tc_fence_after();
         if (it + 1 < n_it) issue_dp(it + 1);
         // dK += dS^T Q, both from shared memory (dS^T K-major, Q MN-major)
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ss(tm + C::TM_DK, sdesc_sw128(sDS + kk * 32, 16, 1024), sdesc_sw128(sQ + kk * 2048, C::Q_ATOM, 1024),
-                 C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u);
-        if (it > 0 && !(ok = mbar_wait(bar(B_DQFREE), (it - 1) & 1, abort_flag, err))) break;
+          mma_ss(tm + C::TM_DK, adv(ds_km, kk * 32), adv(q_mn, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u, issue);
+        if (it > 0 && !(ok = wall(B_DQFREE, (it - 1) & 1))) break;
         tc_fence_after();
         // dQ^T = K^T dS^T
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ss(tm + C::TM_DQ, sdesc_sw128(sK + kk * 2048, C::KV_ATOM, 1024),
-                 sdesc_sw128(sDS + kk * 2048, C::DS_BYTES, 1024), C::ID_DQ, kk > 0);
-        mma_commit(bar(B_DQ));
-        mma_commit(bar(B_EMPTY + s));
-        mma_commit(bar(B_DSFREE + (it & 1)));
+          mma_ss(tm + C::TM_DQ, adv(dK_mn, kk * 2048), adv(ds_mn, kk * 2048), C::ID_DQ, kk > 0, issue);
+        mma_commit(bar(B_DQ), issue);
+        mma_commit(bar(B_EMPTY + s), issue);
+        mma_commit(bar(B_DSFREE + (it & 1)), issue);
         if (it + 2 < n_it) {
           // S^T(it+2) overwrites P(it) in the same buffer: dV(it) must have read it
-          if (!(ok = mbar_wait(bar(B_FULL + (it + 2) % C::STAGES), ((it + 2) / C::STAGES) & 1, abort_flag, err)))
+          if (!(ok = wall(B_FULL + (it + 2) % C::STAGES, ((it + 2) / C::STAGES) & 1)))
             break;
-          if (!(ok = mbar_wait(bar(B_DV), it & 1, abort_flag, err))) break;
+          if (!(ok = wall(B_DV, it & 1))) break;
           tc_fence_after();
           issue_s(it + 2);
         }
       }
       // every MMA issued above must finish before tensor memory is released
-      mma_commit(bar(B_FINAL));
+      mma_commit(bar(B_FINAL), issue);
       mbar_drain(bar(B_FINAL), 0);
     }
   } else if (warp < 10) {
@@ -342,6 +353,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // masking only where the tile needs it: keys past M, or keys past some
     // query of the tile under the causal mask
     const bool tail_keys = m0 + C::BM > p.M;
+    // additive mask: this thread's 32 values (its key row, its 32 query
+    // columns) for the next tile are loaded one tile ahead, as f16 pairs, so
+    // the L2 latency stays off the P computation.  Entries outside the matrix
+    // read as 0; those rows or keys are masked through LSE = +inf or the key
+    // bound anyway.
+    const bool has_mask = p.mask != nullptr;
+    const uint16_t* mrow = p.mask + (m < p.M ? m : 0);
+    uint32_t mk[16];
+    auto load_mask = [&](int itx) {
+      const int64_t nbx = (qt0 + itx % nqt) * C::BQ + hf * 32;
+      const uint16_t* src = mrow + p.M * nbx;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const bool in0 = m < p.M && nbx + 2 * c < p.N, in1 = m < p.M && nbx + 2 * c + 1 < p.N;
+        const uint32_t lo = in0 ? __ldg(src + p.M * (2 * c)) : 0u;
+        const uint32_t hi = in1 ? __ldg(src + p.M * (2 * c + 1)) : 0u;
+        mk[c] = lo | (hi << 16);
+      }
+    };
+    if (has_mask && n_it > 0) load_mask(0);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it % C::STAGES, u = it / C::STAGES;
@@ -366,16 +397,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const int jj = q4 * 4 + e;
           float x = fmaf(__uint_as_float(ra[jj]), c1, -lv[e]);
-          if (p.mask != nullptr) {
-            const int64_t n = nb + jj;
-            const float mv = (m < p.M && n < p.N) ? __half2float(__ushort_as_half(p.mask[m + p.M * n])) : 0.f;
-            x = fmaf(mv, kLog2e, x);
+          if (has_mask) {
+            const uint32_t hbits = (jj & 1) ? (mk[jj >> 1] >> 16) : (mk[jj >> 1] & 0xffffu);
+            x = fmaf(__half2float(__ushort_as_half((unsigned short)hbits)), kLog2e, x);
           }
           if (need_causal && m > nb + jj) x = -INFINITY;
           if (tail_keys && m >= p.M) x = -INFINITY;
           pv[jj] = ex2_approx(x);
         }
       }
+      if (has_mask && it + 1 < n_it) load_mask(it + 1);
       uint32_t pk[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
@@ -449,15 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ dQ drain
     const int dr = (warp & 3) * 32 + lane;  // feature row of dQ^T
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const bool leader = (warp == 10 && lane == 0);
-    float* stage = reinterpret_cast<float*>(smem + C::OFF_DQ);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int64_t h = hkv * rk2 + it / nqt;
       const int64_t n0 = (qt0 + it % nqt) * C::BQ;
       ok = mbar_wait(bar(B_DQ), it & 1, abort_flag, err);
       if (!__all_sync(0xffffffffu, ok)) break;
-      __syncwarp();
       tc_fence_after();
       uint32_t ra[32], rb[32];
       tmem_ld32(tm + lane_off + C::TM_DQ, ra);
@@ -465,31 +493,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait2(ra, rb);
       tc_fence_before();
       mbar_arrive(bar(B_DQFREE));
-      if (it > 0) {
-        ok = mbar_wait(bar(B_STAGEFREE), (it - 1) & 1, abort_flag, err);
-        if (!__all_sync(0xffffffffu, ok)) break;
-      }
       if (dr < D) {
+        float* dst = p.dq + ((b * p.H + h) * p.N + n0) * D + dr;
+        const int64_t rows = (p.N - n0) < C::BQ ? (p.N - n0) : C::BQ;
 #pragma unroll
         for (int jj = 0; jj < 64; ++jj)
-          stage[jj * D + dr] = p.scale * __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(B_STAGED));
-      if (leader) {
-        if (mbar_wait(bar(B_STAGED), it & 1, abort_flag, err)) {
-          const int64_t rows = (p.N - n0) < C::BQ ? (p.N - n0) : C::BQ;
-          if (rows > 0) {
-            bulk_reduce_add_f32(p.dq + ((b * p.H + h) * p.N + n0) * D, sbase + C::OFF_DQ, (uint32_t)(rows * D * 4));
-            bulk_commit_group();
-            bulk_wait_group_read0();
-          }
-          mbar_arrive(bar(B_STAGEFREE));
-        }
+          if (jj < rows) atomicAdd(dst + (int64_t)jj * D, p.scale * __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]));
       }
     }
-    if (leader) bulk_wait_group0();
-    __syncwarp();
     // epilogue: dK rows of this key tile (scaled); collective loads, per-row stores
     const int64_t m = m0 + dr;
     const bool row_ok = m < p.M;

@@ -158,39 +158,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs this loop (descriptors stay warp-uniform); lane 0
+    // issues the MMAs and commits
+    {
+      const uint32_t issue = lane == 0 ? 1u : 0u;
+      auto wall = [&](int i, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, err));
+      };
       const uint32_t sQ = sbase + C::OFF_Q;
       auto issue_s = [&](int j) -> bool {
         const int s = j & 1;
-        if (!mbar_wait(bar(F_FULL + s), (j >> 1) & 1, abort_flag, err)) return false;
+        if (!wall(F_FULL + s, (j >> 1) & 1)) return false;
         // P(j-2) in this tensor-memory buffer must have been consumed
-        if (j >= 2 && !mbar_wait(bar(F_PV + s), ((j >> 1) - 1) & 1, abort_flag, err)) return false;
+        if (j >= 2 && !wall(F_PV + s, ((j >> 1) - 1) & 1)) return false;
         tc_fence_after();
         const uint32_t sK = sbase + C::OFF_K + s * C::ATOMS * C::ATOM;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::ATOM + (kk & 3) * 32;
           mma_ss(tm + C::TM_S + s * 128, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), C::ID_S,
-                 kk > 0);
+                 kk > 0, issue);
         }
-        mma_commit(bar(F_S + s));
+        mma_commit(bar(F_S + s), issue);
         return true;
       };
-      bool ok = mbar_wait(bar(F_Q), 0, abort_flag, err) && issue_s(0);
+      bool ok = wall(F_Q, 0) && issue_s(0);
       for (int j = 0; ok && j < nkv; ++j) {
         const int s = j & 1;
         if (j + 1 < nkv && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait(bar(F_P + s), (j >> 1) & 1, abort_flag, err))) break;
+        if (!(ok = wall(F_P + s, (j >> 1) & 1))) break;
         tc_fence_after();
         const uint32_t sV = sbase + C::OFF_V + s * C::ATOMS * C::ATOM;
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk)
           mma_ts(tm + C::TM_O, tm + C::TM_S + s * 128 + kk * 8, sdesc_sw128(sV + kk * 2048, C::ATOM, 1024), C::ID_PV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(F_PV + s));
-        mma_commit(bar(F_EMPTY + s));
+                 (j > 0 || kk > 0) ? 1u : 0u, issue);
+        mma_commit(bar(F_PV + s), issue);
+        mma_commit(bar(F_EMPTY + s), issue);
       }
-      mma_commit(bar(F_FINAL));
+      mma_commit(bar(F_FINAL), issue);
       mbar_drain(bar(F_FINAL), 0);
     }
   } else {

@@ -227,5 +227,6 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
 FAB_API int fab_last_device_error(fab_stream stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FAB_ERR_CUDA;
   const uint32_t e = take_error_tc() | take_error_fwd();
+  if (e & kErrSmemAlign) return FAB_ERR_CUDA;
   return (e & kErrTimeout) ? FAB_ERR_TIMEOUT : FAB_OK;
 }

@@ -11,6 +11,7 @@ namespace fab {
 
 // Error bits a kernel may OR into its translation unit's device error word.
 constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kErrSmemAlign = 2u;  // dynamic shared memory not 1024-byte aligned
 
 // One validated call, in the units the kernels use.
 struct Problem {

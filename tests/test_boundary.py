@@ -135,3 +135,14 @@ def test_binding_rejects_cpu_tensors(L):
     q = torch.zeros(1, 1, 4, 8)
     with pytest.raises(ValueError):
         binding.fab_forward_lse(q, q, q, None, False, 1.0, q.new_empty(1, 4, 1, 8), q.new_empty(1, 1, 4), None)
+
+
+def test_noalloc_validation_on_host(L):
+    vp = ctypes.c_void_p
+    # B*H*N beyond the fixed scratch: refused before any device work
+    n = binding.NOALLOC_MAX_ROWS // 4 + 1
+    d = binding.make_dims(1, 4, 4, n, 64, 64, 64)
+    rc = L.fab_backward_noalloc(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), None, 0, 1.0,
+                                binding.FAB_BF16, ctypes.byref(d), vp(FAKE), None)
+    assert rc == binding.FAB_ERR_WORKSPACE
+    assert L.fab_backward_noalloc(*([None] * 7), 0, 1.0, 1, None, None, None) == binding.FAB_ERR_INVALID
