@@ -35,6 +35,9 @@ METRIC = "attn-backward TFLOP/s (dQ,dK,dV) and fraction of GB300 dense BF16 peak
 DEFAULT_WORKLOAD = "gqa_causal_d128"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM read + write bytes of one bwd_tc_kernel launch from an ncu capture
+# (profiles/bwd_tc_kernel_gqa_causal_d128.md); replace when the kernel changes.
+MEASURED_TRAFFIC = {"gqa_causal_d128": 622130688 + 316215552}
 
 
 def backward_flops(w: inputs.Workload) -> float:
@@ -349,7 +352,8 @@ def run_fab(args, rank, world, local):
     achieved = flops / (main_mean / 1e3) / 1e12
     peak = float(peaks["bf16_tflops"])
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": args.traffic_bytes,
+                "frac": round(achieved / peak, 4),
+                "traffic": args.traffic_bytes if args.traffic_bytes is not None else MEASURED_TRAFFIC.get(w.name),
                 "kernel": "bwd_tc_kernel" if tensor_core else "dq_simt_kernel+dkdv_simt_kernel",
                 "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone between L2 flushes)"}
 
