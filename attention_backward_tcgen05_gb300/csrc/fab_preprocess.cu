@@ -59,27 +59,56 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ d
   const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const bool vec = (DV % Vec<T>::kElems) == 0;
   const int chunks = DV / Vec<T>::kElems;
-  for (int64_t r0 = gw * rpw; r0 < rows; r0 += warps * rpw) {
-    // r indexes rows of the [DV,H,N,B] layout: r = (b*N + n)*H + h
-    const int64_t r = r0 + lane / lpr;
-    float acc = 0.f;
-    if (r < rows) {
-      const T* dr = d + r * DV;
-      const T* orow = o + r * DV;
-      if (vec) {
-        const uint4* d4 = reinterpret_cast<const uint4*>(dr);
-        const uint4* o4 = reinterpret_cast<const uint4*>(orow);
-        for (int c = sub; c < chunks; c += lpr) acc += Vec<T>::dot(__ldg(d4 + c), __ldg(o4 + c));
-      } else {
-        for (int i = sub; i < DV; i += lpr) acc += to_f32(dr[i]) * to_f32(orow[i]);
+  // Four row groups per pass: all loads are issued before any is reduced, so
+  // each warp keeps several 16-byte requests per lane in flight.
+  constexpr int U = 4;
+  for (int64_t r0 = gw * rpw; r0 < rows; r0 += (int64_t)U * warps * rpw) {
+    float acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[u] = 0.f;
+    if (vec && chunks <= lpr) {  // one 16-byte chunk per lane and row
+      uint4 dv[U], ov[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t r = r0 + (int64_t)u * warps * rpw + lane / lpr;
+        if (r < rows && sub < chunks) {
+          dv[u] = __ldg(reinterpret_cast<const uint4*>(d + r * DV) + sub);
+          ov[u] = __ldg(reinterpret_cast<const uint4*>(o + r * DV) + sub);
+        } else {
+          dv[u] = make_uint4(0, 0, 0, 0);
+          ov[u] = make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = Vec<T>::dot(dv[u], ov[u]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t r = r0 + (int64_t)u * warps * rpw + lane / lpr;
+        if (r >= rows) continue;
+        const T* dr = d + r * DV;
+        const T* orow = o + r * DV;
+        if (vec) {
+          const uint4* d4 = reinterpret_cast<const uint4*>(dr);
+          const uint4* o4 = reinterpret_cast<const uint4*>(orow);
+          for (int c = sub; c < chunks; c += lpr) acc[u] += Vec<T>::dot(__ldg(d4 + c), __ldg(o4 + c));
+        } else {
+          for (int i = sub; i < DV; i += lpr) acc[u] += to_f32(dr[i]) * to_f32(orow[i]);
+        }
       }
     }
-    for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (sub == 0 && r < rows) {
-      const int64_t h = r % H;
-      const int64_t bn = r / H;
-      const int64_t n = bn % N, b = bn / N;
-      di[(b * H + h) * N + n] = acc;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float a = acc[u];
+      for (int off = lpr >> 1; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+      // r indexes rows of the [DV,H,N,B] layout: r = (b*N + n)*H + h
+      const int64_t r = r0 + (int64_t)u * warps * rpw + lane / lpr;
+      if (sub == 0 && r < rows) {
+        const int64_t h = r % H;
+        const int64_t bn = r / H;
+        const int64_t n = bn % N, b = bn / N;
+        di[(b * H + h) * N + n] = a;
+      }
     }
   }
   const int64_t threads = (int64_t)gridDim.x * blockDim.x;
