@@ -359,17 +359,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // read as 0; those rows or keys are masked through LSE = +inf or the key
     // bound anyway.
     const bool has_mask = p.mask != nullptr;
-    const uint16_t* mrow = p.mask + (m < p.M ? m : 0);
+    const bool key_in = m < p.M;
+    const uint16_t* mrow = p.mask + (key_in ? m : 0);
     uint32_t mk[16];
     auto load_mask = [&](int itx) {
       const int64_t nbx = (qt0 + itx % nqt) * C::BQ + hf * 32;
-      const uint16_t* src = mrow + p.M * nbx;
+      const uint16_t* src = mrow + p.M * nbx;  // walks down the query rows
+      if (key_in && nbx + 32 <= p.N) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const bool in0 = m < p.M && nbx + 2 * c < p.N, in1 = m < p.M && nbx + 2 * c + 1 < p.N;
-        const uint32_t lo = in0 ? __ldg(src + p.M * (2 * c)) : 0u;
-        const uint32_t hi = in1 ? __ldg(src + p.M * (2 * c + 1)) : 0u;
-        mk[c] = lo | (hi << 16);
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t lo = __ldg(src);
+          src += p.M;
+          const uint32_t hi = __ldg(src);
+          src += p.M;
+          mk[c] = lo | (hi << 16);
+        }
+      } else {  // key past M or a ragged last query tile
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const bool in0 = key_in && nbx + 2 * c < p.N, in1 = key_in && nbx + 2 * c + 1 < p.N;
+          const uint32_t lo = in0 ? __ldg(src) : 0u;
+          src += p.M;
+          const uint32_t hi = in1 ? __ldg(src) : 0u;
+          src += p.M;
+          mk[c] = lo | (hi << 16);
+        }
       }
     };
     if (has_mask && n_it > 0) load_mask(0);
