@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfab.so")
 
-SOURCES = ["fab_host.cu", "fab_preprocess.cu", "fab_simt.cu", "fab_fwd_tc.cu", "fab_bwd_tc.cu", "fab_noalloc.cu"]
+SOURCES = ["fab_host.cu", "fab_preprocess.cu", "fab_simt.cu", "fab_fwd_tc.cu", "fab_bwd_tc.cu", "fab_dq_tc.cu",
+           "fab_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("fab_device.cuh", "fab_internal.h")] + [os.path.join(INCLUDE, "fab.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,7 +1,8 @@
-// fab_bwd_tc.cu -- the attention backward main kernel on the fifth-generation
-// tensor cores (tcgen05.mma, accumulators in tensor memory, operands staged by
-// TMA in 128-byte-swizzled shared memory).  bf16 inputs, D = DK = DV in
-// {64, 128}, f32 accumulation, f32 packed output.
+// fab_bwd_tc.cu -- the key/value pass of the attention backward on the
+// fifth-generation tensor cores (tcgen05.mma, accumulators in tensor memory,
+// operands staged by TMA in 128-byte-swizzled shared memory).  bf16 inputs,
+// D = DK = DV in {64, 128}, f32 accumulation; writes the dK and dV slices of
+// the packed f32 result.  The query pass (fab_dq_tc.cu) writes dQ.
 //
 // Math (labml "Flash Attention", "Backward pass"; ggmlR attn_ref for the mask
 // and scale): with S = scale * Q K^T + mask, P = exp(S - LSE) (the saved row
@@ -12,9 +13,7 @@
 // batch).  The key/value tile stays in shared memory; the CTA walks every
 // query head of the GQA group and every query tile of BQ = 64 queries
 // (skipping tiles a top-left causal mask empties), so dK and dV of the group
-// accumulate in tensor memory without atomics.  dQ tiles are added into the
-// packed dQ slice (zeroed beforehand) with fire-and-forget f32 reductions
-// (red.global.add) straight from registers.
+// accumulate in tensor memory without atomics.
 //
 // Per query tile, all in the transposed ("key rows") orientation so that one
 // thread owns one key row of every tensor-memory tile:
@@ -26,20 +25,15 @@
 //   dV  += P^T dO     [BM x D]   A = P^T (tmem),         B = dO (smem, MN-major)
 //   dS^T = P^T * (dP^T - D)      -> bf16, smem (128-byte swizzled, key rows)
 //   dK  += dS^T Q     [BM x D]   A = dS^T (smem, K-major), B = Q (smem, MN-major)
-//   dQ^T = K^T dS^T   [D x BQ]   A = K (smem, MN-major), B = dS^T (smem, MN-major)
-// For D = 64 the dQ^T product runs with M = 128 against a zero-filled second
-// half of A, so every product uses the 128-lane accumulator layout.
 //
-// Warp roles (448 threads): warp 0 loads tiles with TMA (and the tile's LSE
+// Warp roles (320 threads): warp 0 loads tiles with TMA (and the tile's LSE
 // and D rows); warp 1 allocates tensor memory and one lane issues every MMA;
 // warps 2-9 turn S and dP into P and dS (thread = key row; two warps share
-// each tensor-memory lane quarter and split the BQ query columns); warps
-// 10-13 drain dQ^T (thread = feature row) and add it into the packed dQ slice
-// (consecutive lanes hit consecutive features, 128 contiguous bytes per warp
-// and query).  All hand-offs are mbarriers; every wait is bounded (see
-// fab_device.cuh).
+// each tensor-memory lane quarter and split the BQ query columns) and write
+// dK and dV at the end.  All hand-offs are mbarriers; every wait is bounded
+// (see fab_device.cuh).
 //
-// Issue order per query tile i: dV(i) | dP^T(i+1), dK(i), dQ^T(i) | S^T(i+2).
+// Issue order per query tile i: dV(i) | dP^T(i+1), dK(i) | S^T(i+2).
 // S^T has two tensor-memory buffers, so scores run two tiles ahead of the
 // softmax warps; dP^T(i+1) is issued as soon as the softmax warps have read
 // dP^T(i) (dS lives in shared memory, so no product reads the dP^T columns).
@@ -56,7 +50,7 @@ namespace {
 __device__ uint32_t g_err_tc;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 448;
+constexpr int kThreads = 320;
 constexpr int kSoftmaxThreads = 256;
 
 template <int D>
@@ -69,8 +63,7 @@ struct Cfg {
   static constexpr uint32_t Q_ATOM = BQ * 128;   // bytes of one atom column of a Q/dO tile
   static constexpr uint32_t DS_BYTES = BM * BQ * 2;
   static constexpr uint32_t OFF_K = 0;
-  static constexpr uint32_t OFF_KZ = OFF_K + ATOMS * KV_ATOM;  // zero atom (D = 64 only)
-  static constexpr uint32_t OFF_V = OFF_KZ + (D == 64 ? KV_ATOM : 0);
+  static constexpr uint32_t OFF_V = OFF_K + ATOMS * KV_ATOM;
   static constexpr uint32_t OFF_Q = OFF_V + ATOMS * KV_ATOM;
   static constexpr uint32_t OFF_DO = OFF_Q + STAGES * ATOMS * Q_ATOM;
   static constexpr uint32_t OFF_DS = OFF_DO + STAGES * ATOMS * Q_ATOM;
@@ -79,11 +72,10 @@ struct Cfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
   static constexpr uint32_t SMEM = OFF_MISC + 64;
   // tensor-memory columns
-  static constexpr uint32_t TM_S0 = 0, TM_DP = 64, TM_DQ = 128, TM_S1 = 192, TM_DV = 256, TM_DK = 256 + D;
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 64, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);
   static constexpr uint32_t ID_DVK = idesc_bf16(128, D, false, true);
-  static constexpr uint32_t ID_DQ = idesc_bf16(128, BQ, true, true);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_DK + D <= TM_COLS, "tensor memory budget");
   static_assert(STAGES <= 4, "barrier slots hold up to four stages");
@@ -100,11 +92,9 @@ enum : int {
   B_DS = 14,
   B_DV = 15,
   B_DK = 16,
-  B_DQ = 17,
-  B_DQFREE = 18,
-  B_DSFREE = 19,  // + buffer
-  B_FINAL = 21,
-  B_COUNT = 22
+  B_DSFREE = 17,  // + buffer
+  B_FINAL = 19,
+  B_COUNT = 20
 };
 static_assert(B_COUNT <= 32, "barrier area holds 32 slots");
 
@@ -115,7 +105,6 @@ struct Params {
   const float* lse;
   const float* di;
   const uint16_t* mask;
-  float* dq;
   float* dk;
   float* dv;
   int kv_tiles;
@@ -171,17 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DS), kSoftmaxThreads);
     mbar_init(bar(B_DV), 1);
     mbar_init(bar(B_DK), 1);
-    mbar_init(bar(B_DQ), 1);
-    mbar_init(bar(B_DQFREE), 128);
     mbar_init(bar(B_DSFREE + 0), 1);
     mbar_init(bar(B_DSFREE + 1), 1);
     mbar_init(bar(B_FINAL), 1);
     fence_mbar_init();
-  }
-  if (D == 64) {  // zero atom behind K: the upper half of the M = 128 dQ^T operand
-    uint4* z = reinterpret_cast<uint4*>(smem + C::OFF_KZ);
-    for (int i = threadIdx.x; i < (int)(C::KV_ATOM / 16); i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), C::TM_COLS);
@@ -260,13 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
       const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);               // K, K-major
       const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);               // V, K-major
-      const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::KV_ATOM, 1024);       // K, MN-major (dQ^T A)
       const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);               // stage 0 Q, K-major
       const uint64_t dQ_mn = sdesc_sw128(sbase + C::OFF_Q, C::Q_ATOM, 1024);        // stage 0 Q, MN-major
       const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
       const uint64_t dO_mn = sdesc_sw128(sbase + C::OFF_DO, C::Q_ATOM, 1024);
       const uint64_t dS_km = sdesc_sw128(sbase + C::OFF_DS, 16, 1024);              // dS^T buffer 0, K-major
-      const uint64_t dS_mn = sdesc_sw128(sbase + C::OFF_DS, C::DS_BYTES, 1024);     // dS^T buffer 0, MN-major
       auto stage_off = [](int it) { return (uint32_t)((it % C::STAGES) * C::ATOMS * C::Q_ATOM); };
       auto s_buf = [&](int it) { return (it & 1) ? C::TM_S1 : C::TM_S0; };
       // packed bf16 P columns: queries 0-31 at +0..15, queries 32-63 at +32..47
@@ -303,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it % C::STAGES;
         const uint64_t o_mn = adv(dO_mn, stage_off(it)), q_mn = adv(dQ_mn, stage_off(it));
-        const uint64_t ds_km = adv(dS_km, (it & 1) * C::DS_BYTES), ds_mn = adv(dS_mn, (it & 1) * C::DS_BYTES);
+        const uint64_t ds_km = adv(dS_km, (it & 1) * C::DS_BYTES);
         // dV += P^T dO, P^T from this tile's score buffer
         if (!(ok = wall(B_P + (it & 1), (it >> 1) & 1))) break;
         tc_fence_after();
@@ -312,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tm + C::TM_DV, tm + s_buf(it) + a_col(kk), adv(o_mn, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u, issue);
         mma_commit(bar(B_DV), issue);
         // dS^T(it) is in shared memory and dP^T(it) has been read: the next
-        // tile's dP^T goes first so its dS work overlaps dK(it) and dQ^T(it)
+        // tile's dP^T goes first so its dS work overlaps dK(it)
         if (!(ok = wall(B_DS, it & 1))) break;
         tc_fence_after();
         if (it + 1 < n_it) issue_dp(it + 1);
@@ -320,13 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
           mma_ss(tm + C::TM_DK, adv(ds_km, kk * 32), adv(q_mn, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u, issue);
-        if (it > 0 && !(ok = wall(B_DQFREE, (it - 1) & 1))) break;
-        tc_fence_after();
-        // dQ^T = K^T dS^T
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ss(tm + C::TM_DQ, adv(dK_mn, kk * 2048), adv(ds_mn, kk * 2048), C::ID_DQ, kk > 0, issue);
-        mma_commit(bar(B_DQ), issue);
         mma_commit(bar(B_EMPTY + s), issue);
         mma_commit(bar(B_DSFREE + (it & 1)), issue);
         if (it + 2 < n_it) {
@@ -342,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar(B_FINAL), issue);
       mbar_drain(bar(B_FINAL), 0);
     }
-  } else if (warp < 10) {
+  } else {
     // ------------------------------------------------------------ softmax / dS
     // warps 2-5 take query columns 0-31 of the tile, warps 6-9 columns 32-63
     const int hf = (warp - 2) >> 2;
@@ -463,80 +436,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();  // the dP^T reads above are done before dP^T(it+1) may overwrite them
       mbar_arrive(bar(B_DS));
     }
-    // epilogue: dV rows of this key tile, half of the columns per warp.  The
-    // tensor-memory loads are warp collectives, so every lane runs them and
-    // only the stores are per row.
+    // epilogue: dV and dK (scaled) rows of this key tile, half of the
+    // columns per warp.  The tensor-memory loads are warp collectives, so
+    // every lane runs them and only the stores are per row.
     const bool row_ok = m < p.M;
-    float* dst = p.dv + ((b * p.Hkv + hkv) * p.M + (row_ok ? m : 0)) * D + hf * (D / 2);
+    const int64_t row = (b * p.Hkv + hkv) * p.M + (row_ok ? m : 0);
+    float* dst_v = p.dv + row * D + hf * (D / 2);
+    float* dst_k = p.dk + row * D + hf * (D / 2);
     if (n_it == 0) {
       if (row_ok)
-        for (int c = 0; c < D / 2; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < D / 2; c += 4) {
+          *reinterpret_cast<float4*>(dst_v + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(dst_k + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     } else {
       const bool done = mbar_wait(bar(B_FINAL), 0, abort_flag, err);
       if (__all_sync(0xffffffffu, done && !*abort_flag)) {
         tc_fence_after();
 #pragma unroll 1
         for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          uint32_t rv[32];
+          uint32_t rv[32], rk[32];
           tmem_ld32(tm + lane_off + C::TM_DV + hf * (D / 2) + c0, rv);
-          tmem_ld_wait(rv);
+          tmem_ld32(tm + lane_off + C::TM_DK + hf * (D / 2) + c0, rk);
+          tmem_ld_wait2(rv, rk);
           if (row_ok) {
 #pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              *reinterpret_cast<float4*>(dst + c0 + c) =
+            for (int c = 0; c < 32; c += 4) {
+              *reinterpret_cast<float4*>(dst_v + c0 + c) =
                   make_float4(__uint_as_float(rv[c]), __uint_as_float(rv[c + 1]), __uint_as_float(rv[c + 2]),
                               __uint_as_float(rv[c + 3]));
-          }
-        }
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ dQ drain
-    const int dr = (warp & 3) * 32 + lane;  // feature row of dQ^T
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int64_t h = hkv * rk2 + it / nqt;
-      const int64_t n0 = (qt0 + it % nqt) * C::BQ;
-      ok = mbar_wait(bar(B_DQ), it & 1, abort_flag, err);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      uint32_t ra[32], rb[32];
-      tmem_ld32(tm + lane_off + C::TM_DQ, ra);
-      tmem_ld32(tm + lane_off + C::TM_DQ + 32, rb);
-      tmem_ld_wait2(ra, rb);
-      tc_fence_before();
-      mbar_arrive(bar(B_DQFREE));
-      if (dr < D) {
-        float* dst = p.dq + ((b * p.H + h) * p.N + n0) * D + dr;
-        const int64_t rows = (p.N - n0) < C::BQ ? (p.N - n0) : C::BQ;
-#pragma unroll
-        for (int jj = 0; jj < 64; ++jj)
-          if (jj < rows) atomicAdd(dst + (int64_t)jj * D, p.scale * __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]));
-      }
-    }
-    // epilogue: dK rows of this key tile (scaled); collective loads, per-row stores
-    const int64_t m = m0 + dr;
-    const bool row_ok = m < p.M;
-    float* dst = p.dk + ((b * p.Hkv + hkv) * p.M + (row_ok ? m : 0)) * D;
-    if (n_it == 0) {
-      if (row_ok)
-        for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      const bool done = mbar_wait(bar(B_FINAL), 0, abort_flag, err);
-      if (__all_sync(0xffffffffu, done && !*abort_flag)) {
-        tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t ra[32];
-          tmem_ld32(tm + lane_off + C::TM_DK + c0, ra);
-          tmem_ld_wait(ra);
-          if (row_ok) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              *reinterpret_cast<float4*>(dst + c0 + c) =
-                  make_float4(p.scale * __uint_as_float(ra[c]), p.scale * __uint_as_float(ra[c + 1]),
-                              p.scale * __uint_as_float(ra[c + 2]), p.scale * __uint_as_float(ra[c + 3]));
+              *reinterpret_cast<float4*>(dst_k + c0 + c) =
+                  make_float4(p.scale * __uint_as_float(rk[c]), p.scale * __uint_as_float(rk[c + 1]),
+                              p.scale * __uint_as_float(rk[c + 2]), p.scale * __uint_as_float(rk[c + 3]));
+            }
           }
         }
       }
@@ -598,7 +530,6 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   p.lse = pr.lse;
   p.di = pr.di;
   p.mask = pr.mask;
-  p.dq = pr.packed;
   p.dk = pr.packed + pr.off_k / 4;
   p.dv = pr.packed + pr.off_v / 4;
   p.kv_tiles = (int)((pr.M + C::BM - 1) / C::BM);
@@ -616,6 +547,7 @@ bool backward_tc_supported(const Problem& p) {
   if (p.DK != 64 && p.DK != 128) return false;
   // TMA coordinates are 32-bit; grid.x must fit as well
   if (p.N >= (1ll << 31) || p.M >= (1ll << 31) || p.H * p.B >= (1ll << 31)) return false;
+  if (((p.N + 127) / 128) * p.H * p.B >= (1ll << 31)) return false;  // query-pass grid
   return true;
 }
 

@@ -1,0 +1,499 @@
+// fab_dq_tc.cu -- the query-gradient pass of the attention backward on the
+// fifth-generation tensor cores.  bf16 inputs, D = DK = DV in {64, 128}, f32
+// accumulation; writes the dQ slice of the packed f32 result.
+//
+// Math (labml "Flash Attention", "Backward pass"; ggmlR attn_ref for the mask
+// and scale): P = exp(scale * Q K^T + mask - LSE), dP = dO V^T,
+// dS = P * (dP - D), dQ = scale * dS K.  D_i = dO_i . O_i comes from the
+// preprocess kernel; LSE from the forward.
+//
+// Decomposition: one CTA per (query tile of 128 rows, query head, batch).  Q
+// and dO stay in shared memory; key tiles stream through a three-stage TMA
+// ring and value tiles through a two-stage one.  dQ accumulates in tensor
+// memory over every key tile and is written once, so this pass needs no
+// atomics and no zero fill.  The key/value pass (fab_bwd_tc.cu) recomputes
+// the same S and dP in the transposed orientation; the two passes write
+// disjoint slices.
+//
+// Per key tile j (thread = query row, 128 tensor-memory lanes):
+//   S    = Q  K_j^T   [128 x 128]  A = Q (smem, K-major),   B = K_j (K-major)
+//   dP   = dO V_j^T   [128 x 128]  A = dO (smem, K-major),  B = V_j (K-major)
+//   dS   = exp2(S*scale*log2e + mask*log2e - LSE*log2e) * (dP - D) -> bf16,
+//          written over the S columns it came from
+//   dQ  += dS K_j     [128 x D]    A = dS (tmem),           B = K_j (MN-major)
+// Three 128-column tensor-memory buffers rotate: tile j's S lands in buffer
+// j % 3, its dP (and then dS, written over dP) in buffer (j + 2) % 3.  P stays
+// in registers, so S(j)'s buffer is free as soon as the softmax warps have
+// read it and dP(j+1) may go there; S(j+2) takes the buffer dQ(j) has
+// finished reading.  Issue order per tile j: dQ(j) | dP(j+2) | S(j+2); the
+// wait for dQ(j) to finish (before S(j+2)) overlaps dP(j+2) in the pipe,
+// and the softmax warps work on tile j+1, whose S and dP were issued one
+// tile earlier.  Each MMA group ends in a single commit (a commit stalls the
+// tensor pipe for about a hundred cycles), which the producer reuses to
+// recycle key and value stages.
+//
+// Warps (320 threads): 0 = TMA producer; 1 = tensor-memory allocator and MMA
+// issuer (lane 0 issues); 2-9 = softmax/dS and the epilogue (two warps per
+// tensor-memory lane quarter, each taking 64 of the tile's 128 keys).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fab.h"
+#include "fab_device.cuh"
+#include "fab_internal.h"
+
+namespace fab {
+namespace {
+
+__device__ uint32_t g_err_dq;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
+
+template <int D>
+struct QCfg {
+  static constexpr int BQ = 128;  // queries per CTA (tensor-memory lanes)
+  static constexpr int BK = 128;  // keys per tile
+  static constexpr int KST = 3;   // key ring stages
+  static constexpr int VST = 2;   // value ring stages
+  static constexpr int ATOMS = D / 64;
+  static constexpr uint32_t ATOM = 128 * 128;  // one 128-row x 128-byte swizzle atom column
+  static constexpr uint32_t TILE = ATOMS * ATOM;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_DO = OFF_Q + TILE;
+  static constexpr uint32_t OFF_K = OFF_DO + TILE;
+  static constexpr uint32_t OFF_V = OFF_K + KST * TILE;
+  static constexpr uint32_t OFF_BAR = OFF_V + VST * TILE;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
+  // +1024 to align the dynamic base; at least 116 KB so one CTA owns an SM
+  // and its whole tensor memory
+  static constexpr uint32_t SMEM_USED = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t SMEM = SMEM_USED > 118784 ? SMEM_USED : 118784;
+  // tensor-memory columns
+  static constexpr uint32_t TM_BUF = 128;  // buffer b at columns 128 b, b = 0, 1, 2
+  static constexpr uint32_t TM_DQ = 384;
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr uint32_t ID_S = idesc_bf16(128, BK, false, false);
+  static constexpr uint32_t ID_DQ = idesc_bf16(128, D, false, true);
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(TM_DQ + D <= TM_COLS, "tensor memory budget");
+};
+
+enum : int {
+  Q_QF = 0,      // Q and dO landed
+  Q_KF = 1,      // + key stage (3)
+  Q_KE = 4,      // + j % 3: dQ(j) finished (buffer (j + 2) % 3 and key stage j % 3 free)
+  Q_VF = 7,      // + value stage (2)
+  Q_S = 11,       // + j % 3: S(j) landed
+  Q_DP = 14,      // + j % 3: dP(j) landed (value stage j % 2 free)
+  Q_PD = 17,      // + j % 3: softmax warps read S(j) (its buffer is free)
+  Q_DS = 20,      // + j % 3: softmax warps wrote dS(j)
+  Q_FINAL = 23,
+  Q_COUNT = 24
+};
+static_assert(Q_COUNT <= 32, "barrier area holds 32 slots");
+
+struct QParams {
+  int64_t B, H, Hkv, N, M;
+  float scale;
+  int causal;
+  const float* lse;
+  const float* di;
+  const uint16_t* mask;
+  float* dq;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                 const QParams p) {
+  using C = QCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
+  uint32_t* err = &g_err_dq;
+
+  const int warp = (int)warp_id();
+  const int lane = (int)lane_id();
+
+  // heavy (late) query tiles first under a causal mask; heads of one GQA
+  // group are adjacent so their key/value tiles are shared through L2
+  const int64_t q_tiles = (p.N + C::BQ - 1) / C::BQ;
+  const int64_t units = p.H * p.B;
+  const int64_t qi = blockIdx.x / units;
+  const int64_t unit = blockIdx.x % units;
+  const int64_t h = unit % p.H, b = unit / p.H;
+  const int64_t hkv = h / (p.H / p.Hkv);
+  const int64_t qt = p.causal ? q_tiles - 1 - qi : qi;
+  const int64_t n0 = qt * C::BQ;
+  int64_t n_kv = (p.M + C::BK - 1) / C::BK;
+  if (p.causal) {
+    const int64_t last = (n0 + C::BQ - 1) / C::BK + 1;  // key tiles holding some m <= n
+    if (last < n_kv) n_kv = last;
+  }
+  const int nkv = (int)n_kv;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    mbar_init(bar(Q_QF), 1);
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(bar(Q_KF + s), 1);
+      mbar_init(bar(Q_KE + s), 1);
+    }
+    for (int s = 0; s < C::VST; ++s) mbar_init(bar(Q_VF + s), 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(bar(Q_S + s), 1);
+      mbar_init(bar(Q_DP + s), 1);
+      mbar_init(bar(Q_PD + s), kSoftmaxThreads);
+      mbar_init(bar(Q_DS + s), kSoftmaxThreads);
+    }
+    mbar_init(bar(Q_FINAL), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nkv > 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmO);
+      mbar_arrive_expect_tx(bar(Q_QF), 2 * C::TILE);
+      for (int a = 0; a < C::ATOMS; ++a) {
+        tma_load_3d(sbase + C::OFF_Q + a * C::ATOM, &tmQ, bar(Q_QF), a * 64, (int)n0, (int)(b * p.H + h));
+        tma_load_4d(sbase + C::OFF_DO + a * C::ATOM, &tmO, bar(Q_QF), a * 64, (int)h, (int)n0, (int)b);
+      }
+      const int kvrow = (int)(b * p.Hkv + hkv);
+      int k_issued = 0, v_issued = 0;
+      static_assert(C::KST == 3 && C::VST == 2, "stage recycling follows the three score buffers");
+      for (int j = 0; j < nkv; ++j) {
+        // value stage j % 2 held V(j-2): free once dP(j-2) finished
+        if (j >= 2 && !mbar_wait(bar(Q_DP + (j - 2) % 3), ((j - 2) / 3) & 1, abort_flag, err)) break;
+        const int vs = j % C::VST;
+        mbar_arrive_expect_tx(bar(Q_VF + vs), C::TILE);
+        for (int a = 0; a < C::ATOMS; ++a)
+          tma_load_3d(sbase + C::OFF_V + vs * C::TILE + a * C::ATOM, &tmV, bar(Q_VF + vs), a * 64, j * C::BK, kvrow);
+        ++v_issued;
+        // key stage j % 3 held K(j-3): free once dQ(j-3) finished
+        if (j >= 3 && !mbar_wait(bar(Q_KE + j % 3), ((j - 3) / 3) & 1, abort_flag, err)) break;
+        const int ks = j % C::KST;
+        mbar_arrive_expect_tx(bar(Q_KF + ks), C::TILE);
+        for (int a = 0; a < C::ATOMS; ++a)
+          tma_load_3d(sbase + C::OFF_K + ks * C::TILE + a * C::ATOM, &tmK, bar(Q_KF + ks), a * 64, j * C::BK, kvrow);
+        ++k_issued;
+      }
+      // let every load started above land before shared memory goes away
+      mbar_drain(bar(Q_QF), 0);
+      for (int j = k_issued > C::KST ? k_issued - C::KST : 0; j < k_issued; ++j)
+        mbar_drain(bar(Q_KF + j % C::KST), (j / C::KST) & 1);
+      for (int j = v_issued > C::VST ? v_issued - C::VST : 0; j < v_issued; ++j)
+        mbar_drain(bar(Q_VF + j % C::VST), (j / C::VST) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // the whole warp runs this code (descriptors stay warp-uniform); lane 0
+    // issues the MMAs and commits
+    if (nkv > 0) {
+      const uint32_t issue = lane == 0 ? 1u : 0u;
+      auto wall = [&](int i, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, err));
+      };
+      // a K step only moves the descriptor's start address (address >> 4 in
+      // the low 14 bits, all addresses < 232 KB), so a step is one add
+      auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
+      const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+      const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);        // key stage 0, K-major
+      const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::ATOM, 1024);   // key stage 0, MN-major
+      const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+      auto kstep = [](int kk) { return (uint32_t)((kk >> 2) * C::ATOM + (kk & 3) * 32); };
+      auto buf = [](int x) { return (uint32_t)(x % 3) * C::TM_BUF; };
+      // packed bf16 dS columns: keys 0-63 at +0..31, keys 64-127 at +64..95
+      auto a_col = [](int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); };
+      auto issue_s = [&](int j) {  // S(j) = Q K_j^T into buffer j
+        const uint64_t kd = adv(dK_km, (j % C::KST) * C::TILE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tm + buf(j), adv(dQ_km, kstep(kk)), adv(kd, kstep(kk)), C::ID_S, kk > 0, issue);
+        mma_commit(bar(Q_S + j % 3), issue);
+      };
+      auto issue_dp = [&](int j) {  // dP(j) = dO V_j^T into buffer j + 2
+        const uint64_t vd = adv(dV_km, (j % C::VST) * C::TILE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tm + buf(j + 2), adv(dO_km, kstep(kk)), adv(vd, kstep(kk)), C::ID_S, kk > 0, issue);
+        mma_commit(bar(Q_DP + j % 3), issue);
+      };
+      auto issue_dq = [&](int j) {  // dQ += dS(j) K_j, dS(j) in buffer j + 2
+        const uint64_t kmn = adv(dK_mn, (j % C::KST) * C::TILE);
+#pragma unroll
+        for (int kk = 0; kk < C::BK / 16; ++kk)
+          mma_ts(tm + C::TM_DQ, tm + buf(j + 2) + a_col(kk), adv(kmn, kk * 2048), C::ID_DQ,
+                 (j > 0 || kk > 0) ? 1u : 0u, issue);
+        mma_commit(bar(Q_KE + j % 3), issue);
+      };
+      // prologue: S(0), S(1), dP(0), dP(1)
+      bool ok = wall(Q_QF, 0) && wall(Q_KF, 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      if (ok && nkv > 1 && (ok = wall(Q_KF + 1, 0))) {
+        tc_fence_after();
+        issue_s(1);
+      }
+      if (ok && (ok = wall(Q_VF, 0))) {
+        tc_fence_after();
+        issue_dp(0);
+      }
+      // dP(1) goes into S(0)'s buffer once the softmax warps have read S(0)
+      if (ok && nkv > 1 && (ok = wall(Q_PD, 0) && wall(Q_VF + 1, 0))) {
+        tc_fence_after();
+        issue_dp(1);
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        // dQ(j) once the softmax warps have written dS(j)
+        if (!(ok = wall(Q_DS + j % 3, (j / 3) & 1))) break;
+        tc_fence_after();
+        issue_dq(j);
+        if (j + 2 < nkv) {
+          // dP(j+2) into S(j+1)'s buffer once the softmax warps have read S(j+1)
+          if (!(ok = wall(Q_PD + (j + 1) % 3, ((j + 1) / 3) & 1))) break;
+          if (!(ok = wall(Q_VF + (j + 2) % C::VST, ((j + 2) / C::VST) & 1))) break;
+          tc_fence_after();
+          issue_dp(j + 2);
+          // S(j+2) overwrites dS(j): dQ(j) must have read it
+          if (!(ok = wall(Q_KF + (j + 2) % C::KST, ((j + 2) / C::KST) & 1))) break;
+          if (!(ok = wall(Q_KE + j % 3, (j / 3) & 1))) break;
+          tc_fence_after();
+          issue_s(j + 2);
+        }
+      }
+      // every MMA issued above must finish before tensor memory is released
+      mma_commit(bar(Q_FINAL), issue);
+      mbar_drain(bar(Q_FINAL), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / dS
+    const int hf = (warp - 2) >> 2;        // warps 2-5: keys 0-63 of a tile, warps 6-9: keys 64-127
+    const int r = (warp & 3) * 32 + lane;  // query row within the tile
+    const int64_t n = n0 + r;
+    const bool row_ok = n < p.N;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float c1 = p.scale * kLog2e;
+    const int64_t rowidx = (b * p.H + h) * p.N + (row_ok ? n : 0);
+    // a row past N (zero-filled Q, dO) gets LSE = +inf, hence P = 0 and dS = 0
+    const float lse2 = row_ok ? p.lse[rowidx] * kLog2e : INFINITY;
+    const float di = row_ok ? p.di[rowidx] : 0.f;
+    // additive mask: this thread's 64 values (its query row, its 64 keys) of
+    // the next tile are loaded one tile ahead, as f16 pairs.  Entries past M
+    // read as 0; those keys are masked by the key bound anyway.
+    const bool has_mask = p.mask != nullptr;
+    const uint16_t* mrow = p.mask + p.M * (row_ok ? n : 0);
+    const bool mvec = (p.M & 7) == 0;  // rows start 16-byte aligned
+    uint32_t mk[32];
+    auto load_mask = [&](int jx) {
+      const int64_t mb = (int64_t)jx * C::BK + hf * 64;
+      if (!row_ok) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) mk[c] = 0u;
+      } else if (mvec && mb + 64 <= p.M) {
+        const uint4* src = reinterpret_cast<const uint4*>(mrow + mb);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = __ldg(src + c);
+          mk[4 * c] = v.x;
+          mk[4 * c + 1] = v.y;
+          mk[4 * c + 2] = v.z;
+          mk[4 * c + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const uint32_t lo = (mb + 2 * c < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c) : 0u;
+          const uint32_t hi = (mb + 2 * c + 1 < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c + 1) : 0u;
+          mk[c] = lo | (hi << 16);
+        }
+      }
+    };
+    if (has_mask && nkv > 0) load_mask(0);
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const uint32_t sb = (uint32_t)(j % 3) * C::TM_BUF, db = (uint32_t)((j + 2) % 3) * C::TM_BUF;
+      const uint32_t ph = (uint32_t)(j / 3) & 1u;
+      const int64_t m0 = (int64_t)j * C::BK;
+      const int64_t mb = m0 + hf * 64;  // first key of this thread's columns
+      ok = mbar_wait(bar(Q_S + j % 3), ph, abort_flag, err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      uint32_t ra[32], rb[32];
+      tmem_ld32(tm + lane_off + sb + hf * 64, ra);
+      tmem_ld32(tm + lane_off + sb + hf * 64 + 32, rb);
+      tmem_ld_wait2(ra, rb);
+      // S(j) is in registers: its buffer may take dP(j+1)
+      tc_fence_before();
+      mbar_arrive(bar(Q_PD + j % 3));
+      float pv[64];
+#pragma unroll
+      for (int e = 0; e < 64; ++e) pv[e] = fmaf(__uint_as_float(e < 32 ? ra[e] : rb[e - 32]), c1, -lse2);
+      if (has_mask) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mk[c]));
+          pv[2 * c] = fmaf(mf.x, kLog2e, pv[2 * c]);
+          pv[2 * c + 1] = fmaf(mf.y, kLog2e, pv[2 * c + 1]);
+        }
+        if (j + 1 < nkv) load_mask(j + 1);
+      }
+      // keys past the causal diagonal (top-left: key m > query n) or past M;
+      // only the diagonal tile and a ragged last tile have any
+      if ((p.causal && m0 + C::BK - 1 > n0) || m0 + C::BK > p.M) {
+        int64_t lim = 63;                              // last allowed column e (key mb + e)
+        if (p.causal && n - mb < lim) lim = n - mb;    // m <= n
+        if (p.M - 1 - mb < lim) lim = p.M - 1 - mb;    // m < M
+        const int li = lim < -1 ? -1 : (int)lim;
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (e > li) pv[e] = -INFINITY;
+      }
+#pragma unroll
+      for (int e = 0; e < 64; ++e) pv[e] = ex2_approx(pv[e]);
+      ok = mbar_wait(bar(Q_DP + j % 3), ph, abort_flag, err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      tmem_ld32(tm + lane_off + db + hf * 64, ra);
+      tmem_ld32(tm + lane_off + db + hf * 64 + 32, rb);
+      tmem_ld_wait2(ra, rb);
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int e = 2 * c;
+        const float d0 = __uint_as_float(e < 32 ? ra[e] : rb[e - 32]);
+        const float d1 = __uint_as_float(e + 1 < 32 ? ra[e + 1] : rb[e + 1 - 32]);
+        pk[c] = pack_bf16x2(pv[e] * (d0 - di), pv[e + 1] * (d1 - di));
+      }
+      // packed dS over the first 32 of this warp's own 64 dP columns (the
+      // other warp of the lane quarter reads only its own columns)
+      tmem_st32(tm + lane_off + db + hf * 64, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(Q_DS + j % 3));
+    }
+    // epilogue: dQ rows of this query tile (scaled), half of the columns per
+    // warp.  The tensor-memory loads are warp collectives, so every lane runs
+    // them and only the stores are per row.
+    float* dst = p.dq + rowidx * D + hf * (D / 2);
+    if (nkv == 0) {
+      if (row_ok)
+        for (int c = 0; c < D / 2; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      const bool done = mbar_wait(bar(Q_FINAL), 0, abort_flag, err);
+      if (__all_sync(0xffffffffu, done && !*abort_flag)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t rv[32];
+          tmem_ld32(tm + lane_off + C::TM_DQ + hf * (D / 2) + c0, rv);
+          tmem_ld_wait(rv);
+          if (row_ok) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              *reinterpret_cast<float4*>(dst + c0 + c) =
+                  make_float4(p.scale * __uint_as_float(rv[c]), p.scale * __uint_as_float(rv[c + 1]),
+                              p.scale * __uint_as_float(rv[c + 2]), p.scale * __uint_as_float(rv[c + 3]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tm, C::TM_COLS);
+  }
+}
+
+bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+              const cuuint32_t* box) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
+  using C = QCfg<D>;
+  CUtensorMap mq, mk, mv, mo;
+  const cuuint64_t e = 2;  // bytes per bf16
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
+    const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.N * D * e};
+    const cuuint32_t box[3] = {64, (cuuint32_t)C::BQ, 1};
+    if (!make_map(&mq, pr.q, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.M, (cuuint64_t)(pr.Hkv * pr.B)};
+    const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.M * D * e};
+    const cuuint32_t box[3] = {64, (cuuint32_t)C::BK, 1};
+    if (!make_map(&mk, pr.k, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mv, pr.v, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    // d [DV,H,N,B]: rows n of one head are H*DV elements apart
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)pr.H, (cuuint64_t)pr.N, (cuuint64_t)pr.B};
+    const cuuint64_t str[3] = {D * e, (cuuint64_t)pr.H * D * e, (cuuint64_t)pr.N * pr.H * D * e};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)C::BQ, 1};
+    if (!make_map(&mo, pr.d, 4, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  QParams p;
+  p.B = pr.B;
+  p.H = pr.H;
+  p.Hkv = pr.Hkv;
+  p.N = pr.N;
+  p.M = pr.M;
+  p.scale = pr.scale;
+  p.causal = pr.causal;
+  p.lse = pr.lse;
+  p.di = pr.di;
+  p.mask = pr.mask;
+  p.dq = pr.packed;
+  const int64_t grid = ((pr.N + C::BQ - 1) / C::BQ) * pr.H * pr.B;
+  cudaError_t err = cudaFuncSetAttribute(dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (err != cudaSuccess) return err;
+  dq_tc_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, p);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dq_tc(const Problem& p, cudaStream_t s) {
+  return p.DK == 128 ? launch_d<128>(p, s) : launch_d<64>(p, s);
+}
+
+uint32_t take_error_dq() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_dq, sizeof(v)) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_err_dq, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace fab

@@ -186,7 +186,7 @@ FAB_API int fab_backward_preprocess(const void* d, const void* o, int dtype, con
   p.o = o;
   p.di = static_cast<float*>(workspace);
   p.packed = packed_out;
-  return from_cuda(launch_preprocess(p, backward_tc_supported(p), static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_preprocess(p, static_cast<cudaStream_t>(stream)));
 }
 
 FAB_API int fab_backward_main(const void* q, const void* k, const void* v, const void* d, const float* lse,
@@ -207,7 +207,10 @@ FAB_API int fab_backward_main(const void* q, const void* k, const void* v, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (backward_tc_supported(p)) {
     if (!encode_tiled_fn()) return FAB_ERR_CUDA;
-    return from_cuda(launch_backward_tc(p, s));
+    // key/value pass (dK, dV), then query pass (dQ); they write disjoint slices
+    rc = from_cuda(launch_backward_tc(p, s));
+    if (rc != FAB_OK) return rc;
+    return from_cuda(launch_dq_tc(p, s));
   }
   return from_cuda(launch_backward_simt(p, s));
 }
@@ -226,7 +229,7 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
 
 FAB_API int fab_last_device_error(fab_stream stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FAB_ERR_CUDA;
-  const uint32_t e = take_error_tc() | take_error_fwd();
+  const uint32_t e = take_error_tc() | take_error_dq() | take_error_fwd();
   if (e & kErrSmemAlign) return FAB_ERR_CUDA;
   return (e & kErrTimeout) ? FAB_ERR_TIMEOUT : FAB_OK;
 }

@@ -32,8 +32,8 @@ struct Problem {
 };
 
 // fab_preprocess.cu: D_i = rowsum(dO * O) into p.di; zero the padding of the
-// packed result and, when zero_dq, the dQ slice.
-cudaError_t launch_preprocess(const Problem& p, bool zero_dq, cudaStream_t s);
+// packed result.
+cudaError_t launch_preprocess(const Problem& p, cudaStream_t s);
 
 // fab_simt.cu: CUDA-core kernels for every dtype and width (DK, DV <= 256).
 cudaError_t launch_forward_simt(const Problem& p, void* o, float* lse, cudaStream_t s);
@@ -43,9 +43,14 @@ cudaError_t launch_backward_simt(const Problem& p, cudaStream_t s);
 bool forward_tc_supported(const Problem& p);
 cudaError_t launch_forward_tc(const Problem& p, void* o, float* lse, cudaStream_t s);
 
-// fab_bwd_tc.cu: the tcgen05 tensor-core backward (bf16, DK == DV in {64, 128}).
+// fab_bwd_tc.cu: the tcgen05 tensor-core backward's key/value pass (dK, dV;
+// bf16, DK == DV in {64, 128}).
 bool backward_tc_supported(const Problem& p);
 cudaError_t launch_backward_tc(const Problem& p, cudaStream_t s);
+
+// fab_dq_tc.cu: the tcgen05 tensor-core backward's query pass (dQ), same
+// problems as launch_backward_tc.
+cudaError_t launch_dq_tc(const Problem& p, cudaStream_t s);
 
 // fab_host.cu: cuTensorMapEncodeTiled from the driver, looked up once.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -56,6 +61,7 @@ EncodeTiledFn encode_tiled_fn();
 // Each kernel translation unit keeps a device error word; these read and
 // clear it (host side, synchronous).
 uint32_t take_error_tc();
+uint32_t take_error_dq();
 uint32_t take_error_fwd();
 
 }  // namespace fab

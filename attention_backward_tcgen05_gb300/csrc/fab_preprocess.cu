@@ -4,8 +4,7 @@
 //   term sum_k P_ik dP_ik rewritten as the dot product of the output row and
 //   its gradient), for every query row (b, h, n), into a f32 [N,H,B] buffer;
 //   plus the zero fill of the packed result's padding (ggmlR packing test: the
-//   whole buffer is zeroed and padding stays 0) and, for the tensor-core path,
-//   of the dQ slice it accumulates into.
+//   whole buffer is zeroed and padding stays 0).
 #include <cuda_bf16.h>
 
 #include "fab.h"
@@ -49,8 +48,8 @@ struct ZeroRange {
 template <typename T>
 __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ d, const T* __restrict__ o,
                                                          float* __restrict__ di, int64_t rows, int DV, int64_t H,
-                                                         int64_t N, int lpr, float4* __restrict__ zero4,
-                                                         int64_t zero4_n, ZeroRange pa, ZeroRange pb, ZeroRange pc) {
+                                                         int64_t N, int lpr, ZeroRange pa, ZeroRange pb,
+                                                         ZeroRange pc) {
   // `lpr` lanes (a power of two) share one row, so a warp covers 32 / lpr rows
   const int lane = threadIdx.x & 31;
   const int sub = lane & (lpr - 1);
@@ -111,10 +110,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ d
       }
     }
   }
-  const int64_t threads = (int64_t)gridDim.x * blockDim.x;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t i = tid; i < zero4_n; i += threads) zero4[i] = z;
   if (tid < pa.n) pa.ptr[tid] = 0.f;
   if (tid < pb.n) pb.ptr[tid] = 0.f;
   if (tid < pc.n) pc.ptr[tid] = 0.f;
@@ -122,18 +118,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ d
 
 }  // namespace
 
-cudaError_t launch_preprocess(const Problem& p, bool zero_dq, cudaStream_t s) {
+cudaError_t launch_preprocess(const Problem& p, cudaStream_t s) {
   const int64_t rows = p.B * p.N * p.H;
   const int64_t nq = p.DK * p.N * p.H * p.B, nk = p.DK * p.M * p.Hkv * p.B, nv = p.DV * p.M * p.Hkv * p.B;
   float* base = p.packed;
-  float4* zero4 = nullptr;
-  int64_t zero4_n = 0;
   ZeroRange pa{base + nq, (int64_t)(p.off_k / 4) - nq};
-  if (zero_dq) {  // dQ slice and its padding: [0, off_k) bytes, a multiple of 16
-    zero4 = reinterpret_cast<float4*>(base);
-    zero4_n = (int64_t)(p.off_k / 16);
-    pa.n = 0;
-  }
   ZeroRange pb{base + p.off_k / 4 + nk, (int64_t)((p.off_v - p.off_k) / 4) - nk};
   ZeroRange pc{base + p.off_v / 4 + nv, (int64_t)((p.end - p.off_v) / 4) - nv};
   int dev = 0, sms = 148;
@@ -148,19 +137,17 @@ cudaError_t launch_preprocess(const Problem& p, bool zero_dq, cudaStream_t s) {
     while (lpr < 32 && lpr < chunks) lpr <<= 1;
   }
   int64_t blocks = (rows * lpr / 32 + 7) / 8 + 1;
-  const int64_t zblocks = (zero4_n + 255) / 256;
-  if (zblocks > blocks) blocks = zblocks;
   const int64_t cap = (int64_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (p.dtype == FAB_BF16) {
     preprocess_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(p.d), static_cast<const __nv_bfloat16*>(p.o), p.di, rows, (int)p.DV, p.H,
-        p.N, lpr, zero4, zero4_n, pa, pb, pc);
+        p.N, lpr, pa, pb, pc);
   } else {
     preprocess_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const float*>(p.d),
                                                               static_cast<const float*>(p.o), p.di, rows, (int)p.DV,
-                                                              p.H, p.N, lpr, zero4, zero4_n, pa, pb, pc);
+                                                              p.H, p.N, lpr, pa, pb, pc);
   }
   return cudaPeekAtLastError();
 }

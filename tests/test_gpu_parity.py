@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from attention_backward_tcgen05_gb300 import binding, inputs
-from parity import TOL, check_pads_zero, compare, oracle_ref, run_gpu
+from parity import TOL, check_pads_zero, compare, oracle_ref, rel_err, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -163,24 +163,46 @@ def test_preprocess_di_and_zero_fill(dtype, DV):
     p = packed.double().cpu().numpy()
     off_k, off_v, end = (t // 4 for t in binding.fab_packed_offsets(dims))
     nq, nk, nv = w.DK * 77 * 6 * 2, w.DK * 50 * 3 * 2, DV * 50 * 3 * 2
-    tensor_core = dtype == "bf16" and w.DK == DV and DV in (64, 128)
-    if tensor_core:  # the dQ slice is zeroed for the reductions
-        assert np.all(p[:off_k] == 0)
-    else:
-        assert np.all(p[:nq] == 7.0) and np.all(p[nq:off_k] == 0)
+    # the preprocess writes D_i and zeroes the padding only: every kernel
+    # writes its gradient slice whole, so the slices keep the fill value
+    assert np.all(p[:nq] == 7.0) and np.all(p[nq:off_k] == 0)
     assert np.all(p[off_k:off_k + nk] == 7.0) and np.all(p[off_k + nk:off_v] == 0)
     assert np.all(p[off_v:off_v + nv] == 7.0) and np.all(p[off_v + nv:] == 0)
 
 
+@pytest.mark.parametrize("D,causal,mask", [(128, True, "none"), (64, False, "random")])
+def test_every_slice_written_over_garbage(D, causal, mask):
+    # the packed buffer starts as NaN: the preprocess zeroes only the padding,
+    # so every gradient element must be written by the kernels themselves
+    w = inputs.custom(2, 4, 2, 200, 300, D, D, causal=causal, mask=mask, seed=31 + D)
+    x = inputs.make(w)
+    dev = torch.device("cuda")
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o, lse = binding.forward(g["q"], g["k"], g["v"], g["mask"], w.causal, w.scale)
+    dims = binding.make_dims(*w.dims)
+    ws, packed = binding.alloc_backward(dims, binding.dtype_code(g["q"]), dev)
+    packed.fill_(float("nan"))
+    binding.fab_backward(g["q"], g["k"], g["v"], g["d"], o, lse, g["mask"], w.causal, w.scale, ws, packed)
+    assert binding.fab_last_device_error() == binding.FAB_OK
+    p = packed.double().cpu().numpy()
+    assert np.all(np.isfinite(p))
+    check_pads_zero(w, p)
+    dq, dk, dv = (t.double().cpu().numpy() for t in binding.unpack(packed, dims))
+    ref = oracle_ref(w, x)
+    for key, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert rel_err(got, ref[key]) <= TOL["bf16"], key
+
+
 def test_many_tiles_repeatable_d128():
     # many query tiles per key tile (GQA group of 4, non-causal) exercises the
-    # double-buffered score tiles and the shared lane quarters; dK and dV do
-    # not use reductions, so repeated runs must agree bit for bit
+    # double-buffered score tiles and the shared lane quarters; no gradient
+    # uses reductions, so repeated runs must agree bit for bit
     w = inputs.custom(1, 4, 1, 1024, 256, 128, seed=21)
     x = inputs.make(w)
     a = run_gpu(w, x)
     b = run_gpu(w, x)
-    assert np.array_equal(a["dk"], b["dk"]) and np.array_equal(a["dv"], b["dv"])
+    for key in ("dq", "dk", "dv"):
+        assert np.array_equal(a[key], b[key]), key
     ref = oracle_ref(w, x)
     errs = compare(w, a, ref)
     assert max(errs["dq"], errs["dk"], errs["dv"]) <= TOL["bf16"], errs
