@@ -6,37 +6,49 @@
 //
 // Math (labml "Flash Attention", "Backward pass"; ggmlR attn_ref for the mask
 // and scale): with S = scale * Q K^T + mask, P = exp(S - LSE) (the saved row
-// log-sum-exp), dV = P^T dO, dP = dO V^T, dS = P * (dP - D), dQ = scale dS K,
-// dK = scale dS^T Q.  D_i = dO_i . O_i comes from the preprocess kernel.
+// log-sum-exp), dV = P^T dO, dP = dO V^T, dS = P * (dP - D), dK = scale dS^T Q.
+// D_i = dO_i . O_i comes from the preprocess kernel.
 //
 // Decomposition: one CTA per (key tile of BM = 128 keys, key/value head,
 // batch).  The key/value tile stays in shared memory; the CTA walks every
-// query head of the GQA group and every query tile of BQ = 64 queries
+// query head of the GQA group and every query tile of BQ = 128 queries
 // (skipping tiles a top-left causal mask empties), so dK and dV of the group
 // accumulate in tensor memory without atomics.
 //
-// Per query tile, all in the transposed ("key rows") orientation so that one
+// Per query tile, in the transposed ("key rows") orientation so that one
 // thread owns one key row of every tensor-memory tile:
 //   S^T  = K  Q^T     [BM x BQ]  A = K (smem, K-major),  B = Q (smem, K-major)
 //   dP^T = V  dO^T    [BM x BQ]  A = V,                  B = dO
-//   P^T  = exp2(S^T * scale*log2e + mask*log2e - LSE*log2e)  -> bf16, tmem
-//          (written over the S^T columns it came from; the dV/dK products
-//          address the two 32-query halves separately)
-//   dV  += P^T dO     [BM x D]   A = P^T (tmem),         B = dO (smem, MN-major)
-//   dS^T = P^T * (dP^T - D)      -> bf16, smem (128-byte swizzled, key rows)
-//   dK  += dS^T Q     [BM x D]   A = dS^T (smem, K-major), B = Q (smem, MN-major)
+//   P^T  = exp2(S^T * scale*log2e + mask*log2e - LSE*log2e)
+//   dS^T = P^T * (dP^T - D)
+//   dV  += P^T dO     [BM x D]   A = P^T (tmem),  B = dO (smem, MN-major)
+//   dK  += dS^T Q     [BM x D]   A = dS^T (tmem), B = Q (smem, MN-major)
+// Every product is an M = 128, N = 128 (or D) MMA: an N = 64 product costs
+// the tensor pipe as long as an N = 128 one.
 //
-// Warp roles (320 threads): warp 0 loads tiles with TMA (and the tile's LSE
-// and D rows); warp 1 allocates tensor memory and one lane issues every MMA;
-// warps 2-9 turn S and dP into P and dS (thread = key row; two warps share
-// each tensor-memory lane quarter and split the BQ query columns) and write
-// dK and dV at the end.  All hand-offs are mbarriers; every wait is bounded
+// Tensor memory (512 columns): two tile buffers X0 at 0 and X1 at 128, dV at
+// 256, dK at 256 + D.  Query tile i lives in X(i % 2) from start to end:
+// S^T(i) lands there; the softmax warps read it into registers (P stays in
+// registers), then dP^T(i) lands in the same columns; a warp reads its 64
+// dP^T columns in two halves of 32 queries and writes each half's P^T and
+// dS^T (packed bf16, 16 columns each) over the 32 columns it just read;
+// dV(i) and dK(i) read them from there.  So dP^T(i) waits only for the
+// softmax warps to read S^T(i), and S^T(i+1) only for dV(i-1), dK(i-1) to
+// finish with the other buffer, while tile i is being worked on.
+//
+// The products are issued by two warps, each waiting only on its own inputs.
+// One issues dP^T(i) once S^T(i) was read, then S^T(i+1) once Q_{i+1} landed
+// and dV(i-1), dK(i-1) are done.  The other issues dV(i) + dK(i) once P^T(i),
+// dS^T(i) are written.  A single issuing thread stalls the tensor pipe for
+// one to two hundred cycles at every commit and barrier wait; with two
+// streams those stalls overlap the other stream's MMAs.
+//
+// Warps (352 threads): 0 = TMA producer (and the tile's LSE and D rows);
+// 1 = tensor-memory allocator and S^T/dP^T issuer; 10 = dV/dK issuer (lane 0
+// of an issuer warp issues); 2-9 = softmax/dS and the epilogue (thread = key
+// row; two warps per tensor-memory lane quarter, each taking 64 of the
+// tile's 128 queries).  All hand-offs are mbarriers; every wait is bounded
 // (see fab_device.cuh).
-//
-// Issue order per query tile i: dV(i) | dP^T(i+1), dK(i) | S^T(i+2).
-// S^T has two tensor-memory buffers, so scores run two tiles ahead of the
-// softmax warps; dP^T(i+1) is issued as soon as the softmax warps have read
-// dP^T(i) (dS lives in shared memory, so no product reads the dP^T columns).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -50,29 +62,30 @@ namespace {
 __device__ uint32_t g_err_tc;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
 
 template <int D>
 struct Cfg {
   static constexpr int BM = 128;  // keys per CTA (tensor-memory lanes)
-  static constexpr int BQ = 64;   // queries per step
-  static constexpr int STAGES = 4;
-  static constexpr int ATOMS = D / 64;  // 128-byte swizzle atoms along D
-  static constexpr uint32_t KV_ATOM = BM * 128;  // bytes of one atom column of a K/V tile
-  static constexpr uint32_t Q_ATOM = BQ * 128;   // bytes of one atom column of a Q/dO tile
-  static constexpr uint32_t DS_BYTES = BM * BQ * 2;
+  static constexpr int BQ = 128;  // queries per step
+  static constexpr int STAGES = D == 128 ? 2 : 4;  // Q/dO ring
+  static constexpr int ATOMS = D / 64;             // 128-byte swizzle atoms along D
+  static constexpr uint32_t ATOM = 128 * 128;      // one 128-row x 128-byte atom column
+  static constexpr uint32_t TILE = ATOMS * ATOM;   // one 128 x D bf16 tile
   static constexpr uint32_t OFF_K = 0;
-  static constexpr uint32_t OFF_V = OFF_K + ATOMS * KV_ATOM;
-  static constexpr uint32_t OFF_Q = OFF_V + ATOMS * KV_ATOM;
-  static constexpr uint32_t OFF_DO = OFF_Q + STAGES * ATOMS * Q_ATOM;
-  static constexpr uint32_t OFF_DS = OFF_DO + STAGES * ATOMS * Q_ATOM;
-  static constexpr uint32_t OFF_LD = OFF_DS + 2 * DS_BYTES;  // per stage: lse2[BQ], D[BQ]
+  static constexpr uint32_t OFF_V = OFF_K + TILE;
+  static constexpr uint32_t OFF_Q = OFF_V + TILE;             // + stage * TILE
+  static constexpr uint32_t OFF_DO = OFF_Q + STAGES * TILE;   // + stage * TILE
+  static constexpr uint32_t OFF_LD = OFF_DO + STAGES * TILE;  // per stage: lse2[BQ], D[BQ]
   static constexpr uint32_t OFF_BAR = OFF_LD + STAGES * 2 * BQ * 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
-  static constexpr uint32_t SMEM = OFF_MISC + 64;
-  // tensor-memory columns
-  static constexpr uint32_t TM_S0 = 0, TM_S1 = 64, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
+  // +1024 to align the dynamic base; at least 116 KB so one CTA owns an SM
+  // and its whole tensor memory
+  static constexpr uint32_t SMEM_USED = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t SMEM = SMEM_USED > 118784 ? SMEM_USED : 118784;
+  // tensor-memory columns: tile buffer b at 128 b (b = 0, 1)
+  static constexpr uint32_t TM_X = 128, TM_DV = 256, TM_DK = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);
   static constexpr uint32_t ID_DVK = idesc_bf16(128, D, false, true);
@@ -84,17 +97,15 @@ struct Cfg {
 // barrier slots
 enum : int {
   B_KV = 0,
-  B_FULL = 1,   // + stage (up to 4)
-  B_EMPTY = 5,  // + stage (up to 4)
-  B_S = 9,      // + S buffer
-  B_DP = 11,
-  B_P = 12,     // + S buffer: per buffer, so warps one tile ahead cannot complete a phase early
-  B_DS = 14,
-  B_DV = 15,
-  B_DK = 16,
-  B_DSFREE = 17,  // + buffer
-  B_FINAL = 19,
-  B_COUNT = 20
+  B_FULL = 1,     // + stage: Q, dO, LSE, D of the stage landed
+  B_XF = 5,       // + stage: dV(i), dK(i) finished (stage i % STAGES and buffer i % 2 free)
+  B_S = 9,        // + i % 2: S^T(i) landed
+  B_SF = 11,      // + i % 2: softmax warps read S^T(i)
+  B_DP = 13,      // + i % 2: dP^T(i) landed
+  B_DS = 15,      // + i % 2: softmax warps wrote P^T(i) and dS^T(i)
+  B_FINAL = 17,   // every dV/dK MMA finished
+  B_FIN_S = 18,   // every S^T and dP^T MMA finished
+  B_COUNT = 19
 };
 static_assert(B_COUNT <= 32, "barrier area holds 32 slots");
 
@@ -107,7 +118,6 @@ struct Params {
   const uint16_t* mask;
   float* dk;
   float* dv;
-  int kv_tiles;
 };
 
 template <int D>
@@ -117,17 +127,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw;
-  if (smem_u32(smem_raw) & 1023u) {  // swizzled tiles need a 1024-byte-aligned base
-    if (threadIdx.x == 0) atomicOr(&g_err_tc, kErrSmemAlign);
-    return;
-  }
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
   float* ld_smem = reinterpret_cast<float*>(smem + C::OFF_LD);
+  uint32_t* err = &g_err_tc;
 
   const int warp = (int)warp_id();
   const int lane = (int)lane_id();
@@ -140,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t m0 = j * C::BM;
   const int64_t rk2 = p.H / p.Hkv;
   const int64_t q_tiles = (p.N + C::BQ - 1) / C::BQ;
-  int64_t qt0 = p.causal ? m0 / C::BQ : 0;
+  int64_t qt0 = p.causal ? m0 / C::BQ : 0;  // first query tile holding some n >= m0
   if (qt0 > q_tiles) qt0 = q_tiles;
   const int64_t nqt = q_tiles - qt0;
   const int n_it = (int)(rk2 * nqt);
@@ -150,19 +157,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_KV), 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(B_FULL + s), 32);
-      mbar_init(bar(B_EMPTY + s), 1);
+      mbar_init(bar(B_XF + s), 1);
     }
-    mbar_init(bar(B_S + 0), 1);
-    mbar_init(bar(B_S + 1), 1);
-    mbar_init(bar(B_DP), 1);
-    mbar_init(bar(B_P + 0), kSoftmaxThreads);
-    mbar_init(bar(B_P + 1), kSoftmaxThreads);
-    mbar_init(bar(B_DS), kSoftmaxThreads);
-    mbar_init(bar(B_DV), 1);
-    mbar_init(bar(B_DK), 1);
-    mbar_init(bar(B_DSFREE + 0), 1);
-    mbar_init(bar(B_DSFREE + 1), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(B_S + x), 1);
+      mbar_init(bar(B_SF + x), kSoftmaxThreads);
+      mbar_init(bar(B_DP + x), 1);
+      mbar_init(bar(B_DS + x), kSoftmaxThreads);
+    }
     mbar_init(bar(B_FINAL), 1);
+    mbar_init(bar(B_FIN_S), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -173,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tmem_holder;
-  uint32_t* err = &g_err_tc;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -184,37 +187,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
         prefetch_tensormap(&tmO);
-        mbar_arrive_expect_tx(bar(B_KV), 2 * C::ATOMS * C::KV_ATOM);
+        mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
         const int kvrow = (int)(b * p.Hkv + hkv);
         for (int a = 0; a < C::ATOMS; ++a) {
-          tma_load_3d(sbase + C::OFF_K + a * C::KV_ATOM, &tmK, bar(B_KV), a * 64, (int)m0, kvrow);
-          tma_load_3d(sbase + C::OFF_V + a * C::KV_ATOM, &tmV, bar(B_KV), a * 64, (int)m0, kvrow);
+          tma_load_3d(sbase + C::OFF_K + a * C::ATOM, &tmK, bar(B_KV), a * 64, (int)m0, kvrow);
+          tma_load_3d(sbase + C::OFF_V + a * C::ATOM, &tmV, bar(B_KV), a * 64, (int)m0, kvrow);
         }
       }
       for (int it = 0; it < n_it; ++it) {
         const int s = it % C::STAGES, u = it / C::STAGES;
-        const bool ok = mbar_wait(bar(B_EMPTY + s), (u & 1) ^ 1, abort_flag, err);
-        if (!__all_sync(0xffffffffu, ok)) break;
         const int64_t h = hkv * rk2 + it / nqt;
         const int64_t n0 = (qt0 + it % nqt) * C::BQ;
         const int64_t rowbase = (b * p.H + h) * p.N;
+        // the tile's LSE and D rows, into registers first: their latency
+        // overlaps the wait for the stage below
+        float lv[C::BQ / 32], dv[C::BQ / 32];
+#pragma unroll
+        for (int k = 0; k < C::BQ / 32; ++k) {
+          const int64_t n = n0 + lane + 32 * k;
+          const bool in = n < p.N;
+          lv[k] = in ? __ldg(p.lse + rowbase + n) * kLog2e : INFINITY;
+          dv[k] = in ? __ldg(p.di + rowbase + n) : 0.f;
+        }
+        // stage s held tile it - STAGES: free once its dV and dK finished
+        const bool ok = it < C::STAGES || mbar_wait(bar(B_XF + s), (u - 1) & 1, abort_flag, err);
+        if (!__all_sync(0xffffffffu, ok)) break;
         float* lds = ld_smem + s * 2 * C::BQ;
         // start the tile copies first; the LSE and D loads below overlap them
         if (lane == 0) {
-          mbar_expect_tx(bar(B_FULL + s), 2 * C::ATOMS * C::Q_ATOM);
+          mbar_expect_tx(bar(B_FULL + s), 2 * C::TILE);
           const int qrow = (int)(b * p.H + h);
           for (int a = 0; a < C::ATOMS; ++a) {
-            tma_load_3d(sbase + C::OFF_Q + (s * C::ATOMS + a) * C::Q_ATOM, &tmQ, bar(B_FULL + s), a * 64, (int)n0,
-                        qrow);
-            tma_load_4d(sbase + C::OFF_DO + (s * C::ATOMS + a) * C::Q_ATOM, &tmO, bar(B_FULL + s), a * 64, (int)h,
+            tma_load_3d(sbase + C::OFF_Q + s * C::TILE + a * C::ATOM, &tmQ, bar(B_FULL + s), a * 64, (int)n0, qrow);
+            tma_load_4d(sbase + C::OFF_DO + s * C::TILE + a * C::ATOM, &tmO, bar(B_FULL + s), a * 64, (int)h,
                         (int)n0, (int)b);
           }
         }
-        for (int jj = lane; jj < C::BQ; jj += 32) {
-          const int64_t n = n0 + jj;
-          const bool in = n < p.N;
-          lds[jj] = in ? p.lse[rowbase + n] * kLog2e : INFINITY;
-          lds[C::BQ + jj] = in ? p.di[rowbase + n] : 0.f;
+#pragma unroll
+        for (int k = 0; k < C::BQ / 32; ++k) {
+          lds[lane + 32 * k] = lv[k];
+          lds[C::BQ + lane + 32 * k] = dv[k];
         }
         // one arrival per lane (count 32) publishes that lane's LSE/D stores
         mbar_arrive(bar(B_FULL + s));
@@ -227,120 +239,106 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = first; it < issued; ++it) mbar_drain(bar(B_FULL + it % C::STAGES), (it / C::STAGES) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // the whole warp runs this loop (descriptors stay warp-uniform); lane 0
-    // issues the MMAs and commits
+  } else if (warp == 1 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // each issuer warp runs its loop convergently (descriptors stay
+    // warp-uniform); lane 0 issues the MMAs and commits
     if (n_it > 0) {
       const uint32_t issue = lane == 0 ? 1u : 0u;
       auto wall = [&](int i, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, err));
       };
-      // Descriptors are built once; a K step only moves the start address,
-      // whose 14-bit field (address >> 4, all addresses < 232 KB) never carries
-      // into the neighbouring fields, so a step is one add.
+      // a K step only moves the descriptor's start address (address >> 4 in
+      // the low 14 bits, all addresses < 232 KB), so a step is one add
       auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
-      const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);               // K, K-major
-      const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);               // V, K-major
-      const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);               // stage 0 Q, K-major
-      const uint64_t dQ_mn = sdesc_sw128(sbase + C::OFF_Q, C::Q_ATOM, 1024);        // stage 0 Q, MN-major
-      const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
-      const uint64_t dO_mn = sdesc_sw128(sbase + C::OFF_DO, C::Q_ATOM, 1024);
-      const uint64_t dS_km = sdesc_sw128(sbase + C::OFF_DS, 16, 1024);              // dS^T buffer 0, K-major
-      auto stage_off = [](int it) { return (uint32_t)((it % C::STAGES) * C::ATOMS * C::Q_ATOM); };
-      auto s_buf = [&](int it) { return (it & 1) ? C::TM_S1 : C::TM_S0; };
-      // packed bf16 P columns: queries 0-31 at +0..15, queries 32-63 at +32..47
-      auto a_col = [](int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); };
-      // byte offset of K step kk inside a K-major tile whose atom columns are `atom` bytes apart
-      auto kstep = [](int kk, uint32_t atom) { return (uint32_t)((kk >> 2) * atom + (kk & 3) * 32); };
-      // S^T(it) = K Q^T into its buffer
-      auto issue_s = [&](int it) {
-        const uint64_t q = adv(dQ_km, stage_off(it));
+      auto kstep = [](int kk) { return (uint32_t)((kk >> 2) * C::ATOM + (kk & 3) * 32); };
+      bool ok = wall(B_KV, 0);
+      if (warp == 1) {
+        // dP^T(i) = V dO_i^T into X(i % 2) once S^T(i) there was read; then
+        // S^T(i+1) = K Q_{i+1}^T into X((i+1) % 2) once Q_{i+1} landed and
+        // dV(i-1), dK(i-1) are done with that buffer
+        const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+        const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+        const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);   // stage 0
+        const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);  // stage 0
+        auto issue_s = [&](int it) {
+          const uint64_t q = adv(dQ_km, (it % C::STAGES) * C::TILE);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tm + s_buf(it), adv(dK_km, kstep(kk, C::KV_ATOM)), adv(q, kstep(kk, C::Q_ATOM)), C::ID_S, kk > 0, issue);
-        mma_commit(bar(B_S + (it & 1)), issue);
-      };
-      // dP^T(it) = V dO^T
-      auto issue_dp = [&](int it) {
-        const uint64_t o = adv(dO_km, stage_off(it));
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tm + C::TM_DP, adv(dV_km, kstep(kk, C::KV_ATOM)), adv(o, kstep(kk, C::Q_ATOM)), C::ID_S, kk > 0, issue);
-        mma_commit(bar(B_DP), issue);
-      };
-      // prologue: S^T(0), dP^T(0), S^T(1)
-      bool ok = wall(B_KV, 0) && wall(B_FULL, 0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
-        if (n_it > 1 && (ok = wall(B_FULL + 1, 0))) {
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tm + (it & 1) * C::TM_X, adv(dK_km, kstep(kk)), adv(q, kstep(kk)), C::ID_S, kk > 0, issue);
+          mma_commit(bar(B_S + (it & 1)), issue);
+        };
+        if ((ok = ok && wall(B_FULL, 0))) {
           tc_fence_after();
-          issue_s(1);
+          issue_s(0);
         }
-      }
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % C::STAGES;
-        const uint64_t o_mn = adv(dO_mn, stage_off(it)), q_mn = adv(dQ_mn, stage_off(it));
-        const uint64_t ds_km = adv(dS_km, (it & 1) * C::DS_BYTES);
-        // dV += P^T dO, P^T from this tile's score buffer
-        if (!(ok = wall(B_P + (it & 1), (it >> 1) & 1))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ts(tm + C::TM_DV, tm + s_buf(it) + a_col(kk), adv(o_mn, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u, issue);
-        mma_commit(bar(B_DV), issue);
-        // dS^T(it) is in shared memory and dP^T(it) has been read: the next
-        // tile's dP^T goes first so its dS work overlaps dK(it)
-        if (!(ok = wall(B_DS, it & 1))) break;
-        tc_fence_after();
-        if (it + 1 < n_it) issue_dp(it + 1);
-        // dK += dS^T Q, both from shared memory (dS^T K-major, Q MN-major)
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ss(tm + C::TM_DK, adv(ds_km, kk * 32), adv(q_mn, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u, issue);
-        mma_commit(bar(B_EMPTY + s), issue);
-        mma_commit(bar(B_DSFREE + (it & 1)), issue);
-        if (it + 2 < n_it) {
-          // S^T(it+2) overwrites P(it) in the same buffer: dV(it) must have read it
-          if (!(ok = wall(B_FULL + (it + 2) % C::STAGES, ((it + 2) / C::STAGES) & 1)))
-            break;
-          if (!(ok = wall(B_DV, it & 1))) break;
+        for (int it = 0; ok && it < n_it; ++it) {
+          if (!(ok = wall(B_SF + (it & 1), (it >> 1) & 1))) break;
           tc_fence_after();
-          issue_s(it + 2);
+          const uint64_t o = adv(dO_km, (it % C::STAGES) * C::TILE);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tm + (it & 1) * C::TM_X, adv(dV_km, kstep(kk)), adv(o, kstep(kk)), C::ID_S, kk > 0, issue);
+          mma_commit(bar(B_DP + (it & 1)), issue);
+          if (it + 1 < n_it) {
+            if (!(ok = wall(B_FULL + (it + 1) % C::STAGES, ((it + 1) / C::STAGES) & 1))) break;
+            if (it > 0 && !(ok = wall(B_XF + (it - 1) % C::STAGES, ((it - 1) / C::STAGES) & 1))) break;
+            tc_fence_after();
+            issue_s(it + 1);
+          }
         }
+        mma_commit(bar(B_FIN_S), issue);
+        mbar_drain(bar(B_FIN_S), 0);
+      } else if (warp == 10) {
+        // dV += P^T dO_i and dK += dS^T Q_i once the softmax warps wrote
+        // P^T(i), dS^T(i) into X: packed bf16, queries 32 g .. 32 g + 31 at
+        // columns 32 g + 0..15 (P) and 32 g + 16..31 (dS)
+        const uint64_t dO_mn = sdesc_sw128(sbase + C::OFF_DO, C::ATOM, 1024);  // stage 0, MN-major
+        const uint64_t dQ_mn = sdesc_sw128(sbase + C::OFF_Q, C::ATOM, 1024);
+        auto p_col = [](int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); };
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int s = it % C::STAGES;
+          if (!(ok = wall(B_DS + (it & 1), (it >> 1) & 1))) break;
+          tc_fence_after();
+          const uint64_t o = adv(dO_mn, s * C::TILE), q = adv(dQ_mn, s * C::TILE);
+          const uint32_t xb = tm + (it & 1) * C::TM_X;
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / 16; ++kk)
+            mma_ts(tm + C::TM_DV, xb + p_col(kk), adv(o, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u, issue);
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / 16; ++kk)
+            mma_ts(tm + C::TM_DK, xb + 16 + p_col(kk), adv(q, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u,
+                   issue);
+          mma_commit(bar(B_XF + s), issue);
+        }
+        // every dV/dK MMA (the last depends on every S^T and dP^T MMA) must
+        // finish before the epilogue reads dV, dK and tensor memory is released
+        mma_commit(bar(B_FINAL), issue);
+        mbar_drain(bar(B_FINAL), 0);
       }
-      // every MMA issued above must finish before tensor memory is released
-      mma_commit(bar(B_FINAL), issue);
-      mbar_drain(bar(B_FINAL), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax / dS
-    // warps 2-5 take query columns 0-31 of the tile, warps 6-9 columns 32-63
+    // warps 2-5 take query columns 0-63 of the tile, warps 6-9 columns 64-127
     const int hf = (warp - 2) >> 2;
     const int r = (warp & 3) * 32 + lane;  // key row within the tile
     const int64_t m = m0 + r;
+    const bool key_in = m < p.M;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c1 = p.scale * kLog2e;
-    // masking only where the tile needs it: keys past M, or keys past some
-    // query of the tile under the causal mask
-    const bool tail_keys = m0 + C::BM > p.M;
-    // additive mask: this thread's 32 values (its key row, its 32 query
-    // columns) for the next tile are loaded one tile ahead, as f16 pairs, so
-    // the L2 latency stays off the P computation.  Entries outside the matrix
-    // read as 0; those rows or keys are masked through LSE = +inf or the key
-    // bound anyway.
+    // additive mask: this thread's 64 values (its key row, its 64 query
+    // columns), as f16 pairs, requested before the tile's score wait so the
+    // L2 latency overlaps it.  Entries outside the matrix read as 0; those
+    // rows or keys are masked through LSE = +inf or the key bound anyway.
     const bool has_mask = p.mask != nullptr;
-    const bool key_in = m < p.M;
     const uint16_t* mrow = p.mask + (key_in ? m : 0);
-    uint32_t mk[16];
+    uint32_t mk[32];
     auto load_mask = [&](int itx) {
-      const int64_t nbx = (qt0 + itx % nqt) * C::BQ + hf * 32;
+      const int64_t nbx = (qt0 + itx % nqt) * C::BQ + hf * 64;
       const uint16_t* src = mrow + p.M * nbx;  // walks down the query rows
-      if (key_in && nbx + 32 <= p.N) {
+      if (key_in && nbx + 64 <= p.N) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < 32; ++c) {
           const uint32_t lo = __ldg(src);
           src += p.M;
           const uint32_t hi = __ldg(src);
@@ -349,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {  // key past M or a ragged last query tile
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < 32; ++c) {
           const bool in0 = key_in && nbx + 2 * c < p.N, in1 = key_in && nbx + 2 * c + 1 < p.N;
           const uint32_t lo = in0 ? __ldg(src) : 0u;
           src += p.M;
@@ -359,92 +357,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    if (has_mask && n_it > 0) load_mask(0);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it % C::STAGES, u = it / C::STAGES;
-      const int64_t nb = (qt0 + it % nqt) * C::BQ + hf * 32;  // first query of this thread's columns
+      const int64_t nb = (qt0 + it % nqt) * C::BQ + hf * 64;  // first query of this thread's columns
+      if (has_mask) load_mask(it);
       ok = mbar_wait(bar(B_FULL + s), u & 1, abort_flag, err);
-      ok = ok && mbar_wait(bar(B_S + (it & 1)), (it >> 1) & 1, abort_flag, err);
+      const uint32_t xb = (uint32_t)(it & 1) * C::TM_X;
+      const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+      ok = ok && mbar_wait(bar(B_S + (it & 1)), ph, abort_flag, err);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const float4* lse4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ + hf * 32);
-      const float4* di4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ + C::BQ + hf * 32);
-      const uint32_t sb = (it & 1) ? C::TM_S1 : C::TM_S0;
-      uint32_t ra[32];
-      tmem_ld32(tm + lane_off + sb + hf * 32, ra);
-      tmem_ld_wait(ra);
-      const bool need_causal = p.causal && (m0 + C::BM - 1 > nb);
-      float pv[32];
+      uint32_t ra[32], rb[32];
+      tmem_ld32(tm + lane_off + xb + hf * 64, ra);
+      tmem_ld32(tm + lane_off + xb + hf * 64 + 32, rb);
+      tmem_ld_wait2(ra, rb);
+      // S^T(i) is in registers: the buffer may take dP^T(i)
+      tc_fence_before();
+      mbar_arrive(bar(B_SF + (it & 1)));
+      const float4* lse4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ + hf * 64);
+      const float4* di4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ + C::BQ + hf * 64);
+      float pv[64];
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
+      for (int q4 = 0; q4 < 16; ++q4) {
         const float4 l4 = lse4[q4];
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int jj = q4 * 4 + e;
-          float x = fmaf(__uint_as_float(ra[jj]), c1, -lv[e]);
-          if (has_mask) {
-            const uint32_t hbits = (jj & 1) ? (mk[jj >> 1] >> 16) : (mk[jj >> 1] & 0xffffu);
-            x = fmaf(__half2float(__ushort_as_half((unsigned short)hbits)), kLog2e, x);
-          }
-          if (need_causal && m > nb + jj) x = -INFINITY;
-          if (tail_keys && m >= p.M) x = -INFINITY;
-          pv[jj] = ex2_approx(x);
+          pv[jj] = fmaf(__uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]), c1, -lv[e]);
         }
       }
-      if (has_mask && it + 1 < n_it) load_mask(it + 1);
-      uint32_t pk[16];
+      if (has_mask) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-      // packed P goes over the first 16 of this warp's own 32 S columns: the
-      // other warp of the lane quarter may still be reading its S columns
-      tmem_st16(tm + lane_off + sb + hf * 32, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(B_P + (it & 1)));
+        for (int c = 0; c < 32; ++c) {
+          const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mk[c]));
+          pv[2 * c] = fmaf(mf.x, kLog2e, pv[2 * c]);
+          pv[2 * c + 1] = fmaf(mf.y, kLog2e, pv[2 * c + 1]);
+        }
+      }
+      // queries before the causal diagonal (top-left: key m > query n) and
+      // keys past M; only diagonal tiles and the last key tile have any
+      if ((p.causal && m0 + C::BM - 1 > nb) || m0 + C::BM > p.M) {
+        int64_t lo = 0;  // first allowed column e (query nb + e)
+        if (p.causal && m - nb > lo) lo = m - nb;
+        if (!key_in) lo = 64;
+        const int li = lo > 64 ? 64 : (int)lo;
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (e < li) pv[e] = -INFINITY;
+      }
+#pragma unroll
+      for (int e = 0; e < 64; ++e) pv[e] = ex2_approx(pv[e]);
 
-      ok = mbar_wait(bar(B_DP), it & 1, abort_flag, err);
+      ok = mbar_wait(bar(B_DP + (it & 1)), ph, abort_flag, err);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      tmem_ld32(tm + lane_off + C::TM_DP + hf * 32, ra);
-      tmem_ld_wait(ra);
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
-        const float4 d4 = di4[q4];
-        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+      for (int g = 0; g < 2; ++g) {
+        // queries 32 g .. 32 g + 31 of this warp's 64: read dP^T, then write
+        // [P^T | dS^T] (16 + 16 packed columns) over the same 32 columns
+        const uint32_t xcol = tm + lane_off + xb + hf * 64 + g * 32;
+        tmem_ld32(xcol, ra);
+        tmem_ld_wait(ra);
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int jj = q4 * 4 + e;
-          pv[jj] = pv[jj] * (__uint_as_float(ra[jj]) - dv[e]);
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 d4 = di4[g * 8 + q4];
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int jj = q4 * 4 + e;  // column within the half
+            const float p0 = pv[g * 32 + jj], p1 = pv[g * 32 + jj + 1];
+            pk[jj >> 1] = pack_bf16x2(p0, p1);
+            pk[16 + (jj >> 1)] =
+                pack_bf16x2(p0 * (__uint_as_float(ra[jj]) - dv[e]), p1 * (__uint_as_float(ra[jj + 1]) - dv[e + 1]));
+          }
         }
+        tmem_st32(xcol, pk);
       }
-#pragma unroll
-      for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-      if (it >= 2) {
-        ok = mbar_wait(bar(B_DSFREE + (it & 1)), ((it >> 1) - 1) & 1, abort_flag, err);
-        if (!__all_sync(0xffffffffu, ok)) break;
-      }
-      // dS^T row r into the swizzled [BM x BQ] bf16 tile (16-byte chunk c of
-      // row r lives at chunk c ^ (r % 8)); this thread owns chunks 4hf..4hf+3
-      const uint32_t rowaddr = sbase + C::OFF_DS + (it & 1) * C::DS_BYTES + r * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        st_shared_v4(rowaddr + (((hf * 4 + c) ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                     pk[4 * c + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();  // the dP^T reads above are done before dP^T(it+1) may overwrite them
-      mbar_arrive(bar(B_DS));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_DS + (it & 1)));
     }
     // epilogue: dV and dK (scaled) rows of this key tile, half of the
     // columns per warp.  The tensor-memory loads are warp collectives, so
     // every lane runs them and only the stores are per row.
-    const bool row_ok = m < p.M;
-    const int64_t row = (b * p.Hkv + hkv) * p.M + (row_ok ? m : 0);
+    const int64_t row = (b * p.Hkv + hkv) * p.M + (key_in ? m : 0);
     float* dst_v = p.dv + row * D + hf * (D / 2);
     float* dst_k = p.dk + row * D + hf * (D / 2);
     if (n_it == 0) {
-      if (row_ok)
+      if (key_in)
         for (int c = 0; c < D / 2; c += 4) {
           *reinterpret_cast<float4*>(dst_v + c) = make_float4(0.f, 0.f, 0.f, 0.f);
           *reinterpret_cast<float4*>(dst_k + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -459,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tm + lane_off + C::TM_DV + hf * (D / 2) + c0, rv);
           tmem_ld32(tm + lane_off + C::TM_DK + hf * (D / 2) + c0, rk);
           tmem_ld_wait2(rv, rk);
-          if (row_ok) {
+          if (key_in) {
 #pragma unroll
             for (int c = 0; c < 32; c += 4) {
               *reinterpret_cast<float4*>(dst_v + c0 + c) =
@@ -532,8 +535,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   p.mask = pr.mask;
   p.dk = pr.packed + pr.off_k / 4;
   p.dv = pr.packed + pr.off_v / 4;
-  p.kv_tiles = (int)((pr.M + C::BM - 1) / C::BM);
-  const int64_t grid = (int64_t)p.kv_tiles * pr.Hkv * pr.B;
+  const int64_t grid = ((pr.M + C::BM - 1) / C::BM) * pr.Hkv * pr.B;
   cudaError_t err = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
   bwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, p);

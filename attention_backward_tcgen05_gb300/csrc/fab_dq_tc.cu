@@ -25,16 +25,20 @@
 // j % 3, its dP (and then dS, written over dP) in buffer (j + 2) % 3.  P stays
 // in registers, so S(j)'s buffer is free as soon as the softmax warps have
 // read it and dP(j+1) may go there; S(j+2) takes the buffer dQ(j) has
-// finished reading.  Issue order per tile j: dQ(j) | dP(j+2) | S(j+2); the
-// wait for dQ(j) to finish (before S(j+2)) overlaps dP(j+2) in the pipe,
-// and the softmax warps work on tile j+1, whose S and dP were issued one
-// tile earlier.  Each MMA group ends in a single commit (a commit stalls the
-// tensor pipe for about a hundred cycles), which the producer reuses to
-// recycle key and value stages.
+// finished reading.
 //
-// Warps (320 threads): 0 = TMA producer; 1 = tensor-memory allocator and MMA
-// issuer (lane 0 issues); 2-9 = softmax/dS and the epilogue (two warps per
-// tensor-memory lane quarter, each taking 64 of the tile's 128 keys).
+// The three products are issued by three warps, one stream each, every one
+// waiting only on its own inputs: S(j) once K_j landed and dQ(j-2) freed its
+// buffer, dP(j) once V_j landed and the softmax warps read S(j-1), dQ(j) once
+// they wrote dS(j).  A single issuing thread stalls the tensor pipe for one
+// to two hundred cycles at every commit and barrier wait; with three streams
+// those stalls overlap other streams' MMAs.  Each group of eight MMAs ends in
+// one commit, which the producer also uses to recycle key and value stages.
+//
+// Warps (384 threads): 0 = TMA producer; 1 = tensor-memory allocator and S
+// issuer; 10 = dP issuer; 11 = dQ issuer (lane 0 of an issuer warp issues);
+// 2-9 = softmax/dS and the epilogue (two warps per tensor-memory lane
+// quarter, each taking 64 of the tile's 128 keys).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -48,7 +52,7 @@ namespace {
 __device__ uint32_t g_err_dq;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
 
 template <int D>
@@ -89,8 +93,10 @@ enum : int {
   Q_DP = 14,      // + j % 3: dP(j) landed (value stage j % 2 free)
   Q_PD = 17,      // + j % 3: softmax warps read S(j) (its buffer is free)
   Q_DS = 20,      // + j % 3: softmax warps wrote dS(j)
-  Q_FINAL = 23,
-  Q_COUNT = 24
+  Q_FINAL = 23,   // every dQ MMA finished
+  Q_FIN_S = 24,   // every S MMA finished
+  Q_FIN_P = 25,   // every dP MMA finished
+  Q_COUNT = 26
 };
 static_assert(Q_COUNT <= 32, "barrier area holds 32 slots");
 
@@ -154,6 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(Q_DS + s), kSoftmaxThreads);
     }
     mbar_init(bar(Q_FINAL), 1);
+    mbar_init(bar(Q_FIN_S), 1);
+    mbar_init(bar(Q_FIN_P), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -203,10 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = v_issued > C::VST ? v_issued - C::VST : 0; j < v_issued; ++j)
         mbar_drain(bar(Q_VF + j % C::VST), (j / C::VST) & 1);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // the whole warp runs this code (descriptors stay warp-uniform); lane 0
-    // issues the MMAs and commits
+  } else if (warp == 1 || warp >= 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // each issuer warp runs its loop convergently (descriptors stay
+    // warp-uniform); lane 0 issues the MMAs and commits
     if (nkv > 0) {
       const uint32_t issue = lane == 0 ? 1u : 0u;
       auto wall = [&](int i, uint32_t parity) {
@@ -215,77 +223,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a K step only moves the descriptor's start address (address >> 4 in
       // the low 14 bits, all addresses < 232 KB), so a step is one add
       auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
-      const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
-      const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
-      const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);        // key stage 0, K-major
-      const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::ATOM, 1024);   // key stage 0, MN-major
-      const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
       auto kstep = [](int kk) { return (uint32_t)((kk >> 2) * C::ATOM + (kk & 3) * 32); };
       auto buf = [](int x) { return (uint32_t)(x % 3) * C::TM_BUF; };
-      // packed bf16 dS columns: keys 0-63 at +0..31, keys 64-127 at +64..95
-      auto a_col = [](int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); };
-      auto issue_s = [&](int j) {  // S(j) = Q K_j^T into buffer j
-        const uint64_t kd = adv(dK_km, (j % C::KST) * C::TILE);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tm + buf(j), adv(dQ_km, kstep(kk)), adv(kd, kstep(kk)), C::ID_S, kk > 0, issue);
-        mma_commit(bar(Q_S + j % 3), issue);
-      };
-      auto issue_dp = [&](int j) {  // dP(j) = dO V_j^T into buffer j + 2
-        const uint64_t vd = adv(dV_km, (j % C::VST) * C::TILE);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tm + buf(j + 2), adv(dO_km, kstep(kk)), adv(vd, kstep(kk)), C::ID_S, kk > 0, issue);
-        mma_commit(bar(Q_DP + j % 3), issue);
-      };
-      auto issue_dq = [&](int j) {  // dQ += dS(j) K_j, dS(j) in buffer j + 2
-        const uint64_t kmn = adv(dK_mn, (j % C::KST) * C::TILE);
-#pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk)
-          mma_ts(tm + C::TM_DQ, tm + buf(j + 2) + a_col(kk), adv(kmn, kk * 2048), C::ID_DQ,
-                 (j > 0 || kk > 0) ? 1u : 0u, issue);
-        mma_commit(bar(Q_KE + j % 3), issue);
-      };
-      // prologue: S(0), S(1), dP(0), dP(1)
-      bool ok = wall(Q_QF, 0) && wall(Q_KF, 0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      if (ok && nkv > 1 && (ok = wall(Q_KF + 1, 0))) {
-        tc_fence_after();
-        issue_s(1);
-      }
-      if (ok && (ok = wall(Q_VF, 0))) {
-        tc_fence_after();
-        issue_dp(0);
-      }
-      // dP(1) goes into S(0)'s buffer once the softmax warps have read S(0)
-      if (ok && nkv > 1 && (ok = wall(Q_PD, 0) && wall(Q_VF + 1, 0))) {
-        tc_fence_after();
-        issue_dp(1);
-      }
-      for (int j = 0; ok && j < nkv; ++j) {
-        // dQ(j) once the softmax warps have written dS(j)
-        if (!(ok = wall(Q_DS + j % 3, (j / 3) & 1))) break;
-        tc_fence_after();
-        issue_dq(j);
-        if (j + 2 < nkv) {
-          // dP(j+2) into S(j+1)'s buffer once the softmax warps have read S(j+1)
-          if (!(ok = wall(Q_PD + (j + 1) % 3, ((j + 1) / 3) & 1))) break;
-          if (!(ok = wall(Q_VF + (j + 2) % C::VST, ((j + 2) / C::VST) & 1))) break;
+      bool ok = wall(Q_QF, 0);
+      if (warp == 1) {
+        // S(j) = Q K_j^T into buffer j, which held dS(j-2)
+        const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+        const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);  // key stage 0, K-major
+        for (int j = 0; ok && j < nkv; ++j) {
+          if (j >= 2 && !(ok = wall(Q_KE + (j - 2) % 3, ((j - 2) / 3) & 1))) break;
+          if (!(ok = wall(Q_KF + j % C::KST, (j / C::KST) & 1))) break;
           tc_fence_after();
-          issue_dp(j + 2);
-          // S(j+2) overwrites dS(j): dQ(j) must have read it
-          if (!(ok = wall(Q_KF + (j + 2) % C::KST, ((j + 2) / C::KST) & 1))) break;
-          if (!(ok = wall(Q_KE + j % 3, (j / 3) & 1))) break;
-          tc_fence_after();
-          issue_s(j + 2);
+          const uint64_t kd = adv(dK_km, (j % C::KST) * C::TILE);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tm + buf(j), adv(dQ_km, kstep(kk)), adv(kd, kstep(kk)), C::ID_S, kk > 0, issue);
+          mma_commit(bar(Q_S + j % 3), issue);
         }
+        mma_commit(bar(Q_FIN_S), issue);
+        mbar_drain(bar(Q_FIN_S), 0);
+      } else if (warp == 10) {
+        // dP(j) = dO V_j^T into buffer j + 2, which held S(j-1)
+        const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+        const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+        for (int j = 0; ok && j < nkv; ++j) {
+          if (j >= 1 && !(ok = wall(Q_PD + (j - 1) % 3, ((j - 1) / 3) & 1))) break;
+          if (!(ok = wall(Q_VF + j % C::VST, (j / C::VST) & 1))) break;
+          tc_fence_after();
+          const uint64_t vd = adv(dV_km, (j % C::VST) * C::TILE);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tm + buf(j + 2), adv(dO_km, kstep(kk)), adv(vd, kstep(kk)), C::ID_S, kk > 0, issue);
+          mma_commit(bar(Q_DP + j % 3), issue);
+        }
+        mma_commit(bar(Q_FIN_P), issue);
+        mbar_drain(bar(Q_FIN_P), 0);
+      } else if (warp == 11) {
+        // dQ += dS(j) K_j, dS(j) in buffer j + 2 (packed bf16: keys 0-63 at
+        // +0..31, keys 64-127 at +64..95), K_j MN-major
+        const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::ATOM, 1024);
+        auto a_col = [](int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); };
+        for (int j = 0; ok && j < nkv; ++j) {
+          if (!(ok = wall(Q_DS + j % 3, (j / 3) & 1))) break;
+          tc_fence_after();
+          const uint64_t kmn = adv(dK_mn, (j % C::KST) * C::TILE);
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk)
+            mma_ts(tm + C::TM_DQ, tm + buf(j + 2) + a_col(kk), adv(kmn, kk * 2048), C::ID_DQ,
+                   (j > 0 || kk > 0) ? 1u : 0u, issue);
+          mma_commit(bar(Q_KE + j % 3), issue);
+        }
+        // every dQ MMA (the last depends on every S and dP MMA) must finish
+        // before the epilogue reads dQ and tensor memory is released
+        mma_commit(bar(Q_FINAL), issue);
+        mbar_drain(bar(Q_FINAL), 0);
       }
-      // every MMA issued above must finish before tensor memory is released
-      mma_commit(bar(Q_FINAL), issue);
-      mbar_drain(bar(Q_FINAL), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax / dS
