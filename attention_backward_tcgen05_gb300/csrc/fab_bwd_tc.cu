@@ -36,6 +36,12 @@
 // softmax warps to read S^T(i), and S^T(i+1) only for dV(i-1), dK(i-1) to
 // finish with the other buffer, while tile i is being worked on.
 //
+// Q and dO stream through separate rings: Q_i is needed first (S^T(i) is
+// issued as soon as the other tile buffer is free), dO_i about a tile later
+// (dP^T(i) after the softmax warps read S^T(i)), so the Q ring is one stage
+// deeper and every load has about a tile to land.  The LSE and D rows of a
+// tile travel with its dO stage.
+//
 // The products are issued by two warps, each waiting only on its own inputs.
 // One issues dP^T(i) once S^T(i) was read, then S^T(i+1) once Q_{i+1} landed
 // and dV(i-1), dK(i-1) are done.  The other issues dV(i) + dK(i) once P^T(i),
@@ -69,20 +75,22 @@ template <int D>
 struct Cfg {
   static constexpr int BM = 128;  // keys per CTA (tensor-memory lanes)
   static constexpr int BQ = 128;  // queries per step
-  static constexpr int STAGES = D == 128 ? 2 : 4;  // Q/dO ring
+  static constexpr int QST = D == 128 ? 3 : 4;  // Q ring
+  static constexpr int OST = D == 128 ? 2 : 4;  // dO ring (with the LSE and D rows)
   static constexpr int ATOMS = D / 64;             // 128-byte swizzle atoms along D
   static constexpr uint32_t ATOM = 128 * 128;      // one 128-row x 128-byte atom column
   static constexpr uint32_t TILE = ATOMS * ATOM;   // one 128 x D bf16 tile
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE;
-  static constexpr uint32_t OFF_Q = OFF_V + TILE;             // + stage * TILE
-  static constexpr uint32_t OFF_DO = OFF_Q + STAGES * TILE;   // + stage * TILE
-  static constexpr uint32_t OFF_LD = OFF_DO + STAGES * TILE;  // per stage: lse2[BQ], D[BQ]
-  static constexpr uint32_t OFF_BAR = OFF_LD + STAGES * 2 * BQ * 4;
+  static constexpr uint32_t OFF_Q = OFF_V + TILE;           // + stage * TILE
+  static constexpr uint32_t OFF_DO = OFF_Q + QST * TILE;    // + stage * TILE
+  static constexpr uint32_t OFF_LD = OFF_DO + OST * TILE;   // per dO stage: lse2[BQ], D[BQ]
+  static constexpr uint32_t OFF_BAR = OFF_LD + OST * 2 * BQ * 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
-  // +1024 to align the dynamic base; at least 116 KB so one CTA owns an SM
-  // and its whole tensor memory
-  static constexpr uint32_t SMEM_USED = OFF_MISC + 64 + 1024;
+  // the swizzled tiles need a 1024-byte-aligned base, checked at run time
+  // (no room for alignment slack at D = 128); at least 116 KB so one CTA
+  // owns an SM and its whole tensor memory
+  static constexpr uint32_t SMEM_USED = OFF_MISC + 64;
   static constexpr uint32_t SMEM = SMEM_USED > 118784 ? SMEM_USED : 118784;
   // tensor-memory columns: tile buffer b at 128 b (b = 0, 1)
   static constexpr uint32_t TM_X = 128, TM_DV = 256, TM_DK = 256 + D;
@@ -91,21 +99,22 @@ struct Cfg {
   static constexpr uint32_t ID_DVK = idesc_bf16(128, D, false, true);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_DK + D <= TM_COLS, "tensor memory budget");
-  static_assert(STAGES <= 4, "barrier slots hold up to four stages");
+  static_assert(QST <= 4 && OST <= QST, "barrier slots hold up to four stages; the dO ring is not deeper");
 };
 
 // barrier slots
 enum : int {
   B_KV = 0,
-  B_FULL = 1,     // + stage: Q, dO, LSE, D of the stage landed
-  B_XF = 5,       // + stage: dV(i), dK(i) finished (stage i % STAGES and buffer i % 2 free)
-  B_S = 9,        // + i % 2: S^T(i) landed
-  B_SF = 11,      // + i % 2: softmax warps read S^T(i)
-  B_DP = 13,      // + i % 2: dP^T(i) landed
-  B_DS = 15,      // + i % 2: softmax warps wrote P^T(i) and dS^T(i)
-  B_FINAL = 17,   // every dV/dK MMA finished
-  B_FIN_S = 18,   // every S^T and dP^T MMA finished
-  B_COUNT = 19
+  B_FQ = 1,       // + i % QST: Q_i landed
+  B_FO = 5,       // + i % OST: dO_i, LSE and D rows of tile i landed
+  B_XF = 9,       // + i % QST: dV(i), dK(i) finished (Q and dO stages of i, buffer i % 2 free)
+  B_S = 13,       // + i % 2: S^T(i) landed
+  B_SF = 15,      // + i % 2: softmax warps read S^T(i)
+  B_DP = 17,      // + i % 2: dP^T(i) landed
+  B_DS = 19,      // + i % 2: softmax warps wrote P^T(i) and dS^T(i)
+  B_FINAL = 21,   // every dV/dK MMA finished
+  B_FIN_S = 22,   // every S^T and dP^T MMA finished
+  B_COUNT = 23
 };
 static_assert(B_COUNT <= 32, "barrier area holds 32 slots");
 
@@ -127,7 +136,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem_raw) & 1023u) {  // swizzled tiles need a 1024-byte-aligned base
+    if (threadIdx.x == 0) atomicOr(&g_err_tc, kErrSmemAlign);
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -155,10 +168,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     mbar_init(bar(B_KV), 1);
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar(B_FULL + s), 32);
+    for (int s = 0; s < C::QST; ++s) {
+      mbar_init(bar(B_FQ + s), 1);
       mbar_init(bar(B_XF + s), 1);
     }
+    for (int s = 0; s < C::OST; ++s) mbar_init(bar(B_FO + s), 32);
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(B_S + x), 1);
       mbar_init(bar(B_SF + x), kSoftmaxThreads);
@@ -194,13 +208,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sbase + C::OFF_V + a * C::ATOM, &tmV, bar(B_KV), a * 64, (int)m0, kvrow);
         }
       }
+      int q_issued = 0;
       for (int it = 0; it < n_it; ++it) {
-        const int s = it % C::STAGES, u = it / C::STAGES;
+        const int qs = it % C::QST, os = it % C::OST;
         const int64_t h = hkv * rk2 + it / nqt;
         const int64_t n0 = (qt0 + it % nqt) * C::BQ;
         const int64_t rowbase = (b * p.H + h) * p.N;
+        const int qrow = (int)(b * p.H + h);
+        // Q stage qs held tile it - QST: free once its dV and dK finished
+        bool ok = it < C::QST || mbar_wait(bar(B_XF + qs), ((it / C::QST) - 1) & 1, abort_flag, err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_FQ + qs), C::TILE);
+          for (int a = 0; a < C::ATOMS; ++a)
+            tma_load_3d(sbase + C::OFF_Q + qs * C::TILE + a * C::ATOM, &tmQ, bar(B_FQ + qs), a * 64, (int)n0, qrow);
+        }
+        ++q_issued;
         // the tile's LSE and D rows, into registers first: their latency
-        // overlaps the wait for the stage below
+        // overlaps the wait for the dO stage below
         float lv[C::BQ / 32], dv[C::BQ / 32];
 #pragma unroll
         for (int k = 0; k < C::BQ / 32; ++k) {
@@ -209,34 +234,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           lv[k] = in ? __ldg(p.lse + rowbase + n) * kLog2e : INFINITY;
           dv[k] = in ? __ldg(p.di + rowbase + n) : 0.f;
         }
-        // stage s held tile it - STAGES: free once its dV and dK finished
-        const bool ok = it < C::STAGES || mbar_wait(bar(B_XF + s), (u - 1) & 1, abort_flag, err);
+        // dO stage os held tile it - OST: free once its dV and dK finished
+        ok = it < C::OST || mbar_wait(bar(B_XF + (it - C::OST) % C::QST), ((it - C::OST) / C::QST) & 1, abort_flag, err);
         if (!__all_sync(0xffffffffu, ok)) break;
-        float* lds = ld_smem + s * 2 * C::BQ;
-        // start the tile copies first; the LSE and D loads below overlap them
         if (lane == 0) {
-          mbar_expect_tx(bar(B_FULL + s), 2 * C::TILE);
-          const int qrow = (int)(b * p.H + h);
-          for (int a = 0; a < C::ATOMS; ++a) {
-            tma_load_3d(sbase + C::OFF_Q + s * C::TILE + a * C::ATOM, &tmQ, bar(B_FULL + s), a * 64, (int)n0, qrow);
-            tma_load_4d(sbase + C::OFF_DO + s * C::TILE + a * C::ATOM, &tmO, bar(B_FULL + s), a * 64, (int)h,
+          mbar_expect_tx(bar(B_FO + os), C::TILE);
+          for (int a = 0; a < C::ATOMS; ++a)
+            tma_load_4d(sbase + C::OFF_DO + os * C::TILE + a * C::ATOM, &tmO, bar(B_FO + os), a * 64, (int)h,
                         (int)n0, (int)b);
-          }
         }
+        float* lds = ld_smem + os * 2 * C::BQ;
 #pragma unroll
         for (int k = 0; k < C::BQ / 32; ++k) {
           lds[lane + 32 * k] = lv[k];
           lds[C::BQ + lane + 32 * k] = dv[k];
         }
         // one arrival per lane (count 32) publishes that lane's LSE/D stores
-        mbar_arrive(bar(B_FULL + s));
+        mbar_arrive(bar(B_FO + os));
         ++issued;
       }
       // let every load this warp started land before shared memory goes away
       if (lane == 0) {
         mbar_drain(bar(B_KV), 0);
-        const int first = issued > C::STAGES ? issued - C::STAGES : 0;
-        for (int it = first; it < issued; ++it) mbar_drain(bar(B_FULL + it % C::STAGES), (it / C::STAGES) & 1);
+        for (int it = q_issued > C::QST ? q_issued - C::QST : 0; it < q_issued; ++it)
+          mbar_drain(bar(B_FQ + it % C::QST), (it / C::QST) & 1);
+        for (int it = issued > C::OST ? issued - C::OST : 0; it < issued; ++it)
+          mbar_drain(bar(B_FO + it % C::OST), (it / C::OST) & 1);
       }
     }
   } else if (warp == 1 || warp == 10) {
@@ -262,27 +285,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);   // stage 0
         const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);  // stage 0
         auto issue_s = [&](int it) {
-          const uint64_t q = adv(dQ_km, (it % C::STAGES) * C::TILE);
+          const uint64_t q = adv(dQ_km, (it % C::QST) * C::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tm + (it & 1) * C::TM_X, adv(dK_km, kstep(kk)), adv(q, kstep(kk)), C::ID_S, kk > 0, issue);
           mma_commit(bar(B_S + (it & 1)), issue);
         };
-        if ((ok = ok && wall(B_FULL, 0))) {
+        if ((ok = ok && wall(B_FQ, 0))) {
           tc_fence_after();
           issue_s(0);
         }
         for (int it = 0; ok && it < n_it; ++it) {
           if (!(ok = wall(B_SF + (it & 1), (it >> 1) & 1))) break;
+          if (!(ok = wall(B_FO + it % C::OST, (it / C::OST) & 1))) break;
           tc_fence_after();
-          const uint64_t o = adv(dO_km, (it % C::STAGES) * C::TILE);
+          const uint64_t o = adv(dO_km, (it % C::OST) * C::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tm + (it & 1) * C::TM_X, adv(dV_km, kstep(kk)), adv(o, kstep(kk)), C::ID_S, kk > 0, issue);
           mma_commit(bar(B_DP + (it & 1)), issue);
           if (it + 1 < n_it) {
-            if (!(ok = wall(B_FULL + (it + 1) % C::STAGES, ((it + 1) / C::STAGES) & 1))) break;
-            if (it > 0 && !(ok = wall(B_XF + (it - 1) % C::STAGES, ((it - 1) / C::STAGES) & 1))) break;
+            if (!(ok = wall(B_FQ + (it + 1) % C::QST, ((it + 1) / C::QST) & 1))) break;
+            if (it > 0 && !(ok = wall(B_XF + (it - 1) % C::QST, ((it - 1) / C::QST) & 1))) break;
             tc_fence_after();
             issue_s(it + 1);
           }
@@ -297,10 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dQ_mn = sdesc_sw128(sbase + C::OFF_Q, C::ATOM, 1024);
         auto p_col = [](int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); };
         for (int it = 0; ok && it < n_it; ++it) {
-          const int s = it % C::STAGES;
           if (!(ok = wall(B_DS + (it & 1), (it >> 1) & 1))) break;
           tc_fence_after();
-          const uint64_t o = adv(dO_mn, s * C::TILE), q = adv(dQ_mn, s * C::TILE);
+          const uint64_t o = adv(dO_mn, (it % C::OST) * C::TILE), q = adv(dQ_mn, (it % C::QST) * C::TILE);
           const uint32_t xb = tm + (it & 1) * C::TM_X;
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 16; ++kk)
@@ -309,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < C::BQ / 16; ++kk)
             mma_ts(tm + C::TM_DK, xb + 16 + p_col(kk), adv(q, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u,
                    issue);
-          mma_commit(bar(B_XF + s), issue);
+          mma_commit(bar(B_XF + it % C::QST), issue);
         }
         // every dV/dK MMA (the last depends on every S^T and dP^T MMA) must
         // finish before the epilogue reads dV, dK and tensor memory is released
@@ -359,10 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int s = it % C::STAGES, u = it / C::STAGES;
+      const int os = it % C::OST;
       const int64_t nb = (qt0 + it % nqt) * C::BQ + hf * 64;  // first query of this thread's columns
       if (has_mask) load_mask(it);
-      ok = mbar_wait(bar(B_FULL + s), u & 1, abort_flag, err);
+      ok = mbar_wait(bar(B_FO + os), (it / C::OST) & 1, abort_flag, err);
       const uint32_t xb = (uint32_t)(it & 1) * C::TM_X;
       const uint32_t ph = (uint32_t)(it >> 1) & 1u;
       ok = ok && mbar_wait(bar(B_S + (it & 1)), ph, abort_flag, err);
@@ -375,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S^T(i) is in registers: the buffer may take dP^T(i)
       tc_fence_before();
       mbar_arrive(bar(B_SF + (it & 1)));
-      const float4* lse4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ + hf * 64);
-      const float4* di4 = reinterpret_cast<const float4*>(ld_smem + s * 2 * C::BQ + C::BQ + hf * 64);
+      const float4* lse4 = reinterpret_cast<const float4*>(ld_smem + os * 2 * C::BQ + hf * 64);
+      const float4* di4 = reinterpret_cast<const float4*>(ld_smem + os * 2 * C::BQ + C::BQ + hf * 64);
       float pv[64];
 #pragma unroll
       for (int q4 = 0; q4 < 16; ++q4) {
