@@ -11,9 +11,10 @@
 //
 // Decomposition: one CTA per (key tile of BM = 128 keys, key/value head,
 // batch).  The key/value tile stays in shared memory; the CTA walks every
-// query head of the GQA group and every query tile of BQ = 128 queries
-// (skipping tiles a top-left causal mask empties), so dK and dV of the group
-// accumulate in tensor memory without atomics.
+// query tile of BQ = 128 queries (skipping tiles a top-left causal mask
+// empties) and, for each, every query head of the GQA group, so dK and dV of
+// the group accumulate in tensor memory without atomics and the additive
+// mask tile (shared by all heads) is read once per query tile.
 //
 // Per query tile, in the transposed ("key rows") orientation so that one
 // thread owns one key row of every tensor-memory tile:
@@ -211,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int qs = it % C::QST, os = it % C::OST;
-        const int64_t h = hkv * rk2 + it / nqt;
-        const int64_t n0 = (qt0 + it % nqt) * C::BQ;
+        const int64_t h = hkv * rk2 + it % rk2;
+        const int64_t n0 = (qt0 + it / rk2) * C::BQ;
         const int64_t rowbase = (b * p.H + h) * p.N;
         const int qrow = (int)(b * p.H + h);
         // Q stage qs held tile it - QST: free once its dV and dK finished
@@ -350,14 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c1 = p.scale * kLog2e;
     // additive mask: this thread's 64 values (its key row, its 64 query
-    // columns), as f16 pairs, requested before the tile's score wait so the
-    // L2 latency overlaps it.  Entries outside the matrix read as 0; those
-    // rows or keys are masked through LSE = +inf or the key bound anyway.
+    // columns), as f16 pairs, loaded once per query tile (the first head of
+    // the group) and kept for the others.  Entries outside the matrix read as
+    // 0; those rows or keys are masked through LSE = +inf or the key bound
+    // anyway.
     const bool has_mask = p.mask != nullptr;
     const uint16_t* mrow = p.mask + (key_in ? m : 0);
     uint32_t mk[32];
     auto load_mask = [&](int itx) {
-      const int64_t nbx = (qt0 + itx % nqt) * C::BQ + hf * 64;
+      const int64_t nbx = (qt0 + itx / rk2) * C::BQ + hf * 64;
       const uint16_t* src = mrow + p.M * nbx;  // walks down the query rows
       if (key_in && nbx + 64 <= p.N) {
 #pragma unroll
@@ -383,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int os = it % C::OST;
-      const int64_t nb = (qt0 + it % nqt) * C::BQ + hf * 64;  // first query of this thread's columns
-      if (has_mask) load_mask(it);
+      const int64_t nb = (qt0 + it / rk2) * C::BQ + hf * 64;  // first query of this thread's columns
+      if (has_mask && it % rk2 == 0) load_mask(it);
       ok = mbar_wait(bar(B_FO + os), (it / C::OST) & 1, abort_flag, err);
       const uint32_t xb = (uint32_t)(it & 1) * C::TM_X;
       const uint32_t ph = (uint32_t)(it >> 1) & 1u;
