@@ -92,6 +92,9 @@ struct Cfg {
   // (no room for alignment slack at D = 128); at least 116 KB so one CTA
   // owns an SM and its whole tensor memory
   static constexpr uint32_t SMEM_USED = OFF_MISC + 64;
+  // epilogue staging of dV and dK (f32, 32-column atoms), over the tiles
+  static constexpr uint32_t OFF_STAGE = 0;
+  static constexpr uint32_t STAGE_DK = (D / 32) * ATOM;
   static constexpr uint32_t SMEM = SMEM_USED > 118784 ? SMEM_USED : 118784;
   // tensor-memory columns: tile buffer b at 128 b (b = 0, 1)
   static constexpr uint32_t TM_X = 128, TM_DV = 256, TM_DK = 256 + D;
@@ -100,6 +103,7 @@ struct Cfg {
   static constexpr uint32_t ID_DVK = idesc_bf16(128, D, false, true);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_DK + D <= TM_COLS, "tensor memory budget");
+  static_assert(OFF_STAGE + 2 * STAGE_DK <= OFF_LD, "dV/dK staging fits the tile area");
   static_assert(QST <= 4 && OST <= QST, "barrier slots hold up to four stages; the dO ring is not deeper");
 };
 
@@ -134,6 +138,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                   const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -465,41 +470,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(B_DS + (it & 1)));
     }
-    // epilogue: dV and dK (scaled) rows of this key tile, half of the
-    // columns per warp.  The tensor-memory loads are warp collectives, so
-    // every lane runs them and only the stores are per row.
-    const int64_t row = (b * p.Hkv + hkv) * p.M + (key_in ? m : 0);
-    float* dst_v = p.dv + row * D + hf * (D / 2);
-    float* dst_k = p.dk + row * D + hf * (D / 2);
-    if (n_it == 0) {
-      if (key_in)
-        for (int c = 0; c < D / 2; c += 4) {
-          *reinterpret_cast<float4*>(dst_v + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(dst_k + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    } else {
-      const bool done = mbar_wait(bar(B_FINAL), 0, abort_flag, err);
-      if (__all_sync(0xffffffffu, done && !*abort_flag)) {
-        tc_fence_after();
+    // epilogue: dV and dK (scaled) of this key tile, half of the columns per
+    // warp, staged in the now idle tile area (dV from 0, dK from D * 512
+    // bytes) as 32-column atoms of 128-byte swizzled rows, then written by
+    // bulk tensor stores (rows past M are clipped by the store).  The
+    // tensor-memory loads are warp collectives, so every lane runs them.
+    const bool done = n_it > 0 && mbar_wait(bar(B_FINAL), 0, abort_flag, err);
+    const bool write = __all_sync(0xffffffffu, done && !*abort_flag);
+    if (write) {
+      tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          uint32_t rv[32], rk[32];
-          tmem_ld32(tm + lane_off + C::TM_DV + hf * (D / 2) + c0, rv);
-          tmem_ld32(tm + lane_off + C::TM_DK + hf * (D / 2) + c0, rk);
-          tmem_ld_wait2(rv, rk);
-          if (key_in) {
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t rv[32], rk[32];
+        tmem_ld32(tm + lane_off + C::TM_DV + hf * (D / 2) + c0, rv);
+        tmem_ld32(tm + lane_off + C::TM_DK + hf * (D / 2) + c0, rk);
+        tmem_ld_wait2(rv, rk);
+        const uint32_t rowv = sbase + C::OFF_STAGE + (uint32_t)((hf * (D / 2) + c0) / 32) * C::ATOM + r * 128;
+        const uint32_t rowk = rowv + C::STAGE_DK;
 #pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              *reinterpret_cast<float4*>(dst_v + c0 + c) =
-                  make_float4(__uint_as_float(rv[c]), __uint_as_float(rv[c + 1]), __uint_as_float(rv[c + 2]),
-                              __uint_as_float(rv[c + 3]));
-              *reinterpret_cast<float4*>(dst_k + c0 + c) =
-                  make_float4(p.scale * __uint_as_float(rk[c]), p.scale * __uint_as_float(rk[c + 1]),
-                              p.scale * __uint_as_float(rk[c + 2]), p.scale * __uint_as_float(rk[c + 3]));
-            }
-          }
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k ^ (r & 7)) << 4;
+          st_shared_v4(rowv + off, rv[4 * k], rv[4 * k + 1], rv[4 * k + 2], rv[4 * k + 3]);
+          st_shared_v4(rowk + off, __float_as_uint(p.scale * __uint_as_float(rk[4 * k])),
+                       __float_as_uint(p.scale * __uint_as_float(rk[4 * k + 1])),
+                       __float_as_uint(p.scale * __uint_as_float(rk[4 * k + 2])),
+                       __float_as_uint(p.scale * __uint_as_float(rk[4 * k + 3])));
         }
       }
+      fence_proxy_async_smem();
+    } else if (n_it == 0 && key_in) {
+      // no query reaches these keys: dK = dV = 0
+      const int64_t row = (b * p.Hkv + hkv) * p.M + m;
+      float* dst_v = p.dv + row * D + hf * (D / 2);
+      float* dst_k = p.dk + row * D + hf * (D / 2);
+      for (int c = 0; c < D / 2; c += 4) {
+        *reinterpret_cast<float4*>(dst_v + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(dst_k + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    named_bar_sync(1, kSoftmaxThreads);
+    if (warp == 2 && lane == 0 && write) {
+      const int kvrow = (int)(b * p.Hkv + hkv);
+      for (int a = 0; a < D / 32; ++a) {
+        tma_store_3d(&tmDV, sbase + C::OFF_STAGE + a * C::ATOM, a * 32, (int)m0, kvrow);
+        tma_store_3d(&tmDK, sbase + C::OFF_STAGE + C::STAGE_DK + a * C::ATOM, a * 32, (int)m0, kvrow);
+      }
+      bulk_commit_group();
+      bulk_wait_all();
     }
   }
 
@@ -512,20 +529,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box) {
+              const cuuint32_t* box, bool f32 = false) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides,
-                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                   const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 template <int D>
 cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   using C = Cfg<D>;
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mdk, mdv;
   const cuuint64_t e = 2;  // bytes per bf16
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
@@ -547,6 +564,14 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)C::BQ, 1};
     if (!make_map(&mo, pr.d, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
+  {
+    // the packed f32 dK and dV slices [D,M,Hkv,B], stored in 32-column (128-byte) boxes
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.M, (cuuint64_t)(pr.Hkv * pr.B)};
+    const cuuint64_t str[2] = {D * 4, (cuuint64_t)pr.M * D * 4};
+    const cuuint32_t box[3] = {32, (cuuint32_t)C::BM, 1};
+    if (!make_map(&mdk, pr.packed + pr.off_k / 4, 3, dims, str, box, true)) return cudaErrorInvalidValue;
+    if (!make_map(&mdv, pr.packed + pr.off_v / 4, 3, dims, str, box, true)) return cudaErrorInvalidValue;
+  }
   Params p;
   p.B = pr.B;
   p.H = pr.H;
@@ -563,7 +588,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   const int64_t grid = ((pr.M + C::BM - 1) / C::BM) * pr.Hkv * pr.B;
   cudaError_t err = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  bwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, p);
+  bwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdk, mdv, p);
   return cudaPeekAtLastError();
 }
 

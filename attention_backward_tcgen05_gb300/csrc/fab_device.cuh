@@ -1,5 +1,5 @@
 // fab_device.cuh -- sm_103a device helpers: mbarriers with bounded waits, TMA
-// tensor loads, bulk reductions, and the tcgen05 tensor-core / tensor-memory
+// tensor loads and stores, and the tcgen05 tensor-core / tensor-memory
 // instructions, written as inline PTX.
 #pragma once
 
@@ -107,6 +107,27 @@ FAB_DEV void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int
       "%6}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
+}
+
+// Tiled bulk store shared -> global (bulk-group completion).  Coordinates
+// outside the tensor are clipped: those elements are not written.
+FAB_DEV void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+FAB_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until every bulk store this thread committed has completed (global
+// writes done, shared memory free).
+FAB_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Barrier among `count` threads (a multiple of 32) on hardware barrier `id`
+// (id 0 is __syncthreads).
+FAB_DEV void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 FAB_DEV void prefetch_tensormap(const CUtensorMap* map) {

@@ -82,6 +82,7 @@ struct QCfg {
   static constexpr uint32_t ID_DQ = idesc_bf16(128, D, false, true);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_DQ + D <= TM_COLS, "tensor memory budget");
+  static_assert(OFF_Q == 0 && OFF_DO == TILE && D * 128 * 4 <= 2 * TILE, "dQ staging fits the Q and dO tiles");
 };
 
 enum : int {
@@ -114,7 +115,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                 const QParams p) {
+                 const __grid_constant__ CUtensorMap tmDQ, const QParams p) {
   using C = QCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -385,31 +386,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(Q_DS + j % 3));
     }
-    // epilogue: dQ rows of this query tile (scaled), half of the columns per
-    // warp.  The tensor-memory loads are warp collectives, so every lane runs
-    // them and only the stores are per row.
-    float* dst = p.dq + rowidx * D + hf * (D / 2);
-    if (nkv == 0) {
-      if (row_ok)
-        for (int c = 0; c < D / 2; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      const bool done = mbar_wait(bar(Q_FINAL), 0, abort_flag, err);
-      if (__all_sync(0xffffffffu, done && !*abort_flag)) {
-        tc_fence_after();
+    // epilogue: dQ of this query tile (scaled), half of the columns per
+    // warp, staged in the now idle Q/dO area as 32-column atoms of 128-byte
+    // swizzled rows, then written by bulk tensor stores (rows past N are
+    // clipped by the store).  The tensor-memory loads are warp collectives,
+    // so every lane runs them.
+    const bool done = nkv > 0 && mbar_wait(bar(Q_FINAL), 0, abort_flag, err);
+    const bool write = __all_sync(0xffffffffu, done && !*abort_flag);
+    if (write) {
+      tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          uint32_t rv[32];
-          tmem_ld32(tm + lane_off + C::TM_DQ + hf * (D / 2) + c0, rv);
-          tmem_ld_wait(rv);
-          if (row_ok) {
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t rv[32];
+        tmem_ld32(tm + lane_off + C::TM_DQ + hf * (D / 2) + c0, rv);
+        tmem_ld_wait(rv);
+        const uint32_t row = sbase + C::OFF_Q + (uint32_t)((hf * (D / 2) + c0) / 32) * C::ATOM + r * 128;
 #pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              *reinterpret_cast<float4*>(dst + c0 + c) =
-                  make_float4(p.scale * __uint_as_float(rv[c]), p.scale * __uint_as_float(rv[c + 1]),
-                              p.scale * __uint_as_float(rv[c + 2]), p.scale * __uint_as_float(rv[c + 3]));
-          }
-        }
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(row + ((k ^ (r & 7)) << 4), __float_as_uint(p.scale * __uint_as_float(rv[4 * k])),
+                       __float_as_uint(p.scale * __uint_as_float(rv[4 * k + 1])),
+                       __float_as_uint(p.scale * __uint_as_float(rv[4 * k + 2])),
+                       __float_as_uint(p.scale * __uint_as_float(rv[4 * k + 3])));
       }
+      fence_proxy_async_smem();
+    } else if (nkv == 0 && row_ok) {
+      float* dst = p.dq + rowidx * D + hf * (D / 2);
+      for (int c = 0; c < D / 2; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    named_bar_sync(1, kSoftmaxThreads);
+    if (warp == 2 && lane == 0 && write) {
+      for (int a = 0; a < D / 32; ++a)
+        tma_store_3d(&tmDQ, sbase + C::OFF_Q + a * C::ATOM, a * 32, (int)n0, (int)(b * p.H + h));
+      bulk_commit_group();
+      bulk_wait_all();
     }
   }
 
@@ -422,19 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box) {
+              const cuuint32_t* box, bool f32 = false) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D>
 cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   using C = QCfg<D>;
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mdq;
   const cuuint64_t e = 2;  // bytes per bf16
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
@@ -456,6 +466,13 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)C::BQ, 1};
     if (!make_map(&mo, pr.d, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
+  {
+    // the packed f32 dQ slice [D,N,H,B], stored in 32-column (128-byte) boxes
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
+    const cuuint64_t str[2] = {D * 4, (cuuint64_t)pr.N * D * 4};
+    const cuuint32_t box[3] = {32, (cuuint32_t)C::BQ, 1};
+    if (!make_map(&mdq, pr.packed, 3, dims, str, box, true)) return cudaErrorInvalidValue;
+  }
   QParams p;
   p.B = pr.B;
   p.H = pr.H;
@@ -471,7 +488,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   const int64_t grid = ((pr.N + C::BQ - 1) / C::BQ) * pr.H * pr.B;
   cudaError_t err = cudaFuncSetAttribute(dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  dq_tc_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, p);
+  dq_tc_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdq, p);
   return cudaPeekAtLastError();
 }
 
