@@ -27,7 +27,8 @@ FAB_F32, FAB_BF16 = 0, 1
 
 EXPORTS = ("fab_version", "fab_status_string", "fab_packed_offsets", "fab_packed_bytes",
            "fab_backward_workspace_bytes", "fab_forward_lse", "fab_backward", "fab_backward_preprocess",
-           "fab_backward_main", "fab_backward_noalloc", "fab_last_device_error")
+           "fab_backward_main", "fab_backward_query_pass", "fab_backward_key_pass", "fab_backward_noalloc",
+           "fab_last_device_error")
 NOALLOC_MAX_ROWS = 1048576  # FAB_NOALLOC_MAX_ROWS
 
 
@@ -70,6 +71,8 @@ def lib():
                     "fab_backward": ([vp, vp, vp, vp, vp, vp, vp, i32, f32, i32, dp, vp, sz, vp, vp], i32),
                     "fab_backward_preprocess": ([vp, vp, i32, dp, vp, sz, vp, vp], i32),
                     "fab_backward_main": ([vp, vp, vp, vp, vp, vp, i32, f32, i32, dp, vp, sz, vp, vp], i32),
+                    "fab_backward_query_pass": ([vp, vp, vp, vp, vp, vp, vp, i32, f32, i32, dp, vp, sz, vp, vp], i32),
+                    "fab_backward_key_pass": ([vp, vp, vp, vp, vp, vp, i32, f32, i32, dp, vp, sz, vp, vp], i32),
                     "fab_backward_noalloc": ([vp, vp, vp, vp, vp, vp, vp, i32, f32, i32, dp, vp, vp], i32),
                     "fab_last_device_error": ([vp], i32),
                 }
@@ -200,6 +203,32 @@ def fab_backward_main(q, k, v, d, lse, mask, causal, scale, workspace, packed_ou
             workspace.numel() * workspace.element_size(),
             _dev(packed_out, "packed_out", torch.float32, (fab_packed_bytes(dims) // 4,)), _stream(stream))
     _check(lib().fab_backward_main(*args), "fab_backward_main")
+
+
+def fab_backward_query_pass(q, k, v, d, o, lse, mask, causal, scale, workspace, packed_out, stream=None):
+    """Tensor-core query pass: D_i into the workspace, the dQ slice and the padding."""
+    dims = dims_of(q, k, v)
+    t = dtype_code(q)
+    oshape = (dims.B, dims.N, dims.H, dims.DV)
+    args = (_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), _dev(d, "d", q.dtype, oshape),
+            _dev(o, "o", q.dtype, oshape), _dev(lse, "lse", torch.float32, (dims.B, dims.H, dims.N)),
+            _mask(mask, dims), int(bool(causal)), float(scale), t, ctypes.byref(dims),
+            _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+            _dev(packed_out, "packed_out", torch.float32, (fab_packed_bytes(dims) // 4,)), _stream(stream))
+    _check(lib().fab_backward_query_pass(*args), "fab_backward_query_pass")
+
+
+def fab_backward_key_pass(q, k, v, d, lse, mask, causal, scale, workspace, packed_out, stream=None):
+    """Tensor-core key/value pass: the dK and dV slices (D_i read from the workspace)."""
+    dims = dims_of(q, k, v)
+    t = dtype_code(q)
+    args = (_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype),
+            _dev(d, "d", q.dtype, (dims.B, dims.N, dims.H, dims.DV)),
+            _dev(lse, "lse", torch.float32, (dims.B, dims.H, dims.N)), _mask(mask, dims), int(bool(causal)),
+            float(scale), t, ctypes.byref(dims), _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(),
+            _dev(packed_out, "packed_out", torch.float32, (fab_packed_bytes(dims) // 4,)), _stream(stream))
+    _check(lib().fab_backward_key_pass(*args), "fab_backward_key_pass")
 
 
 def fab_backward_noalloc(q, k, v, d, o, lse, mask, causal, scale, packed_out, stream=None):

@@ -4,8 +4,10 @@
 //
 // Math (labml "Flash Attention", "Backward pass"; ggmlR attn_ref for the mask
 // and scale): P = exp(scale * Q K^T + mask - LSE), dP = dO V^T,
-// dS = P * (dP - D), dQ = scale * dS K.  D_i = dO_i . O_i comes from the
-// preprocess kernel; LSE from the forward.
+// dS = P * (dP - D), dQ = scale * dS K; LSE from the forward.  D_i = dO_i .
+// O_i either comes from the preprocess kernel or, when the kernel is built
+// with FUSE_D, is computed here (each row's dO is in shared memory anyway)
+// and written out for the key/value pass, which then runs after this one.
 //
 // Decomposition: one CTA per (query tile of 128 rows, query head, batch).  Q
 // and dO stay in shared memory; key tiles stream through a three-stage TMA
@@ -72,7 +74,8 @@ struct QCfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
   // +1024 to align the dynamic base; at least 116 KB so one CTA owns an SM
   // and its whole tensor memory
-  static constexpr uint32_t SMEM_USED = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t OFF_DPART = OFF_MISC + 64;  // D_i partial sums, 2 x BQ floats
+  static constexpr uint32_t SMEM_USED = OFF_DPART + 2 * BQ * 4 + 1024;
   static constexpr uint32_t SMEM = SMEM_USED > 118784 ? SMEM_USED : 118784;
   // tensor-memory columns
   static constexpr uint32_t TM_BUF = 128;  // buffer b at columns 128 b, b = 0, 1, 2
@@ -106,12 +109,15 @@ struct QParams {
   float scale;
   int causal;
   const float* lse;
-  const float* di;
+  float* di;  // read, or written with FUSE_D
   const uint16_t* mask;
   float* dq;
+  const __nv_bfloat16* o;  // forward output [D,H,N,B], read with FUSE_D
+  float* pad[3];           // the packed result's padding after each slice, zeroed with FUSE_D
+  int pad_n[3];
 };
 
-template <int D>
+template <int D, bool FUSE_D>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -291,7 +297,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t rowidx = (b * p.H + h) * p.N + (row_ok ? n : 0);
     // a row past N (zero-filled Q, dO) gets LSE = +inf, hence P = 0 and dS = 0
     const float lse2 = row_ok ? p.lse[rowidx] * kLog2e : INFINITY;
-    const float di = row_ok ? p.di[rowidx] : 0.f;
+    float di;
+    if (FUSE_D) {
+      // D_i = dO_i . O_i: this thread takes columns hf * D/2 .. hf * D/2 + D/2 - 1
+      // of its row (O from global, dO from the swizzled tile in shared memory);
+      // the two halves meet in shared memory
+      uint4 ov[D / 16];
+      const uint4* orow = reinterpret_cast<const uint4*>(p.o + ((b * p.N + (row_ok ? n : 0)) * p.H + h) * D + hf * (D / 2));
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) ov[c] = row_ok ? __ldg(orow + c) : make_uint4(0, 0, 0, 0);
+      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(Q_QF), 0, abort_flag, err));
+      float part = 0.f;
+      if (got) {
+        auto dot2 = [](uint32_t a, uint32_t b) {
+          return __uint_as_float(a << 16) * __uint_as_float(b << 16) +
+                 __uint_as_float(a & 0xffff0000u) * __uint_as_float(b & 0xffff0000u);
+        };
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          const int e = hf * (D / 2) + 8 * c;  // first column of the 16-byte chunk
+          const uint4 dv = ld_shared_v4(sbase + C::OFF_DO + (uint32_t)(e / 64) * C::ATOM + r * 128 +
+                                        ((((e % 64) / 8) ^ (r & 7)) << 4));
+          part += dot2(dv.x, ov[c].x) + dot2(dv.y, ov[c].y) + dot2(dv.z, ov[c].z) + dot2(dv.w, ov[c].w);
+        }
+      }
+      float* dpart = reinterpret_cast<float*>(smem + C::OFF_DPART);
+      dpart[hf * C::BQ + r] = part;
+      named_bar_sync(2, kSoftmaxThreads);
+      di = dpart[r] + dpart[C::BQ + r];
+      if (hf == 0 && row_ok) p.di[rowidx] = di;
+      if (blockIdx.x == 0 && warp == 2 && lane == 0)
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+          for (int i = 0; i < p.pad_n[k]; ++i) p.pad[k][i] = 0.f;
+    } else {
+      di = row_ok ? p.di[rowidx] : 0.f;
+    }
     // additive mask: this thread's 64 values (its query row, its 64 keys) of
     // the next tile are loaded one tile ahead, as f16 pairs.  Entries past M
     // read as 0; those keys are masked by the key bound anyway.
@@ -441,7 +482,7 @@ bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* di
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool FUSE_D>
 cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   using C = QCfg<D>;
   CUtensorMap mq, mk, mv, mo, mdq;
@@ -485,17 +526,29 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   p.di = pr.di;
   p.mask = pr.mask;
   p.dq = pr.packed;
+  p.o = static_cast<const __nv_bfloat16*>(pr.o);
+  {
+    const int64_t nq = D * pr.N * pr.H * pr.B, nk = D * pr.M * pr.Hkv * pr.B;
+    p.pad[0] = pr.packed + nq;
+    p.pad_n[0] = (int)(pr.off_k / 4 - nq);
+    p.pad[1] = pr.packed + pr.off_k / 4 + nk;
+    p.pad_n[1] = (int)((pr.off_v - pr.off_k) / 4 - nk);
+    p.pad[2] = pr.packed + pr.off_v / 4 + nk;
+    p.pad_n[2] = (int)((pr.end - pr.off_v) / 4 - nk);
+  }
   const int64_t grid = ((pr.N + C::BQ - 1) / C::BQ) * pr.H * pr.B;
-  cudaError_t err = cudaFuncSetAttribute(dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t err =
+      cudaFuncSetAttribute(dq_tc_kernel<D, FUSE_D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  dq_tc_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdq, p);
+  dq_tc_kernel<D, FUSE_D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdq, p);
   return cudaPeekAtLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_dq_tc(const Problem& p, cudaStream_t s) {
-  return p.DK == 128 ? launch_d<128>(p, s) : launch_d<64>(p, s);
+cudaError_t launch_dq_tc(const Problem& p, bool fuse_d, cudaStream_t s) {
+  if (fuse_d) return p.DK == 128 ? launch_d<128, true>(p, s) : launch_d<64, true>(p, s);
+  return p.DK == 128 ? launch_d<128, false>(p, s) : launch_d<64, false>(p, s);
 }
 
 uint32_t take_error_dq() {

@@ -207,12 +207,65 @@ FAB_API int fab_backward_main(const void* q, const void* k, const void* v, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (backward_tc_supported(p)) {
     if (!encode_tiled_fn()) return FAB_ERR_CUDA;
-    // key/value pass (dK, dV), then query pass (dQ); they write disjoint slices
-    rc = from_cuda(launch_backward_tc(p, s));
+    // query pass (dQ), then key/value pass (dK, dV); they write disjoint slices
+    rc = from_cuda(launch_dq_tc(p, false, s));
     if (rc != FAB_OK) return rc;
-    return from_cuda(launch_dq_tc(p, s));
+    return from_cuda(launch_backward_tc(p, s));
   }
   return from_cuda(launch_backward_simt(p, s));
+}
+
+namespace {
+
+// The tensor-core problem of a validated backward call (fab_backward's
+// arguments); false when the tensor-core kernels do not cover it.
+bool tc_problem(const void* q, const void* k, const void* v, const void* d, const void* o, const float* lse,
+                const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims, void* workspace,
+                float* packed_out, Problem* out) {
+  Problem p = make_problem(dims, dtype, scale, causal);
+  if (!backward_tc_supported(p)) return false;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.d = d;
+  p.o = o;
+  p.lse = lse;
+  p.mask = mask;
+  p.di = static_cast<float*>(workspace);
+  p.packed = packed_out;
+  *out = p;
+  return true;
+}
+
+}  // namespace
+
+FAB_API int fab_backward_query_pass(const void* q, const void* k, const void* v, const void* d, const void* o,
+                                    const float* lse, const uint16_t* mask, int causal, float scale, int dtype,
+                                    const fab_dims* dims, void* workspace, size_t workspace_bytes, float* packed_out,
+                                    fab_stream stream) {
+  const void* ptrs[6] = {q, k, v, d, o, lse};
+  int rc = check_backward(dims, dtype, ptrs, 6, mask, workspace, workspace_bytes, packed_out);
+  if (rc != FAB_OK) return rc;
+  Problem p;
+  if (!tc_problem(q, k, v, d, o, lse, mask, causal, scale, dtype, dims, workspace, packed_out, &p))
+    return FAB_ERR_UNSUPPORTED;
+  if (!encode_tiled_fn()) return FAB_ERR_CUDA;
+  return from_cuda(launch_dq_tc(p, true, static_cast<cudaStream_t>(stream)));
+}
+
+FAB_API int fab_backward_key_pass(const void* q, const void* k, const void* v, const void* d, const float* lse,
+                                  const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims,
+                                  const void* workspace, size_t workspace_bytes, float* packed_out,
+                                  fab_stream stream) {
+  const void* ptrs[5] = {q, k, v, d, lse};
+  int rc = check_backward(dims, dtype, ptrs, 5, mask, workspace, workspace_bytes, packed_out);
+  if (rc != FAB_OK) return rc;
+  Problem p;
+  if (!tc_problem(q, k, v, d, nullptr, lse, mask, causal, scale, dtype, dims, const_cast<void*>(workspace),
+                  packed_out, &p))
+    return FAB_ERR_UNSUPPORTED;
+  if (!encode_tiled_fn()) return FAB_ERR_CUDA;
+  return from_cuda(launch_backward_tc(p, static_cast<cudaStream_t>(stream)));
 }
 
 FAB_API int fab_backward(const void* q, const void* k, const void* v, const void* d, const void* o, const float* lse,
@@ -221,6 +274,16 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
   const void* ptrs[6] = {q, k, v, d, o, lse};
   int rc = check_backward(dims, dtype, ptrs, 6, mask, workspace, workspace_bytes, packed_out);
   if (rc != FAB_OK) return rc;
+  Problem p;
+  if (tc_problem(q, k, v, d, o, lse, mask, causal, scale, dtype, dims, workspace, packed_out, &p)) {
+    // the query pass computes D_i itself (and zeroes the padding), then the
+    // key/value pass reads it: two launches, no preprocess
+    rc = fab_backward_query_pass(q, k, v, d, o, lse, mask, causal, scale, dtype, dims, workspace, workspace_bytes,
+                                 packed_out, stream);
+    if (rc != FAB_OK) return rc;
+    return fab_backward_key_pass(q, k, v, d, lse, mask, causal, scale, dtype, dims, workspace, workspace_bytes,
+                                 packed_out, stream);
+  }
   rc = fab_backward_preprocess(d, o, dtype, dims, workspace, workspace_bytes, packed_out, stream);
   if (rc != FAB_OK) return rc;
   return fab_backward_main(q, k, v, d, lse, mask, causal, scale, dtype, dims, workspace, workspace_bytes, packed_out,

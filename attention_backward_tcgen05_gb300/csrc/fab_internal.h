@@ -49,8 +49,10 @@ bool backward_tc_supported(const Problem& p);
 cudaError_t launch_backward_tc(const Problem& p, cudaStream_t s);
 
 // fab_dq_tc.cu: the tcgen05 tensor-core backward's query pass (dQ), same
-// problems as launch_backward_tc.
-cudaError_t launch_dq_tc(const Problem& p, cudaStream_t s);
+// problems as launch_backward_tc.  With fuse_d it also computes D_i from p.o
+// into p.di and zeroes the packed result's padding (the preprocess's work);
+// otherwise it reads D_i from p.di.
+cudaError_t launch_dq_tc(const Problem& p, bool fuse_d, cudaStream_t s);
 
 // fab_host.cu: cuTensorMapEncodeTiled from the driver, looked up once.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

@@ -1,12 +1,16 @@
 """Benchmark: attention backward TFLOP/s on GB300 through libfab's C ABI.
 
-One step = one fab_backward over the workload (D_i preprocess + the main
-gradient kernel), inputs resident in HBM, L2 flushed (256 MiB write) before
-every step.  Throughput counts 10*B*H*N*M*D flops per backward, halved for a
-causal mask.  Also reported: the main kernel's share (roofline against the
-measured dense bf16 peak), an end-to-end number with host buffers (pinned
-H2D copies of the inputs, the backward, D2H of the packed gradients), the
-forward kernel's TFLOP/s, and the fp64 CPU oracle timed on a bounded sample.
+One step = one backward over the workload, inputs resident in HBM, L2
+flushed (256 MiB write) before every step.  On the tensor-core path a step
+is fab_backward_query_pass (D_i and dQ) then fab_backward_key_pass (dK, dV),
+exactly what fab_backward enqueues, with a CUDA event between the two so
+each kernel's launch time is measured; elsewhere it is
+fab_backward_preprocess then fab_backward_main.  Throughput counts
+10*B*H*N*M*D flops per backward, halved for a causal mask.  Also reported:
+the dominant kernel's roofline against the measured dense bf16 peak, an
+end-to-end number with host buffers (pinned H2D copies of the inputs,
+fab_backward, D2H of the packed gradients), the forward kernel's TFLOP/s,
+and the fp64 CPU oracle timed on a bounded sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl fab|reference]
 
@@ -35,13 +39,22 @@ METRIC = "attn-backward TFLOP/s (dQ,dK,dV) and fraction of GB300 dense BF16 peak
 DEFAULT_WORKLOAD = "gqa_causal_d128"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM read + write bytes of one bwd_tc_kernel launch from an ncu capture
-# (profiles/bwd_tc_kernel_gqa_causal_d128.md); replace when the kernel changes.
-MEASURED_TRAFFIC = {"gqa_causal_d128": 622130688 + 316215552}
+# DRAM read + write bytes of one launch of the dominant kernel from an ncu
+# capture (profiles/), keyed by workload; entries are removed when the kernel
+# changes after the capture.
+MEASURED_TRAFFIC = {}
 
 
 def backward_flops(w: inputs.Workload) -> float:
     f = 10.0 * w.B * w.H * w.N * w.M * w.DK
+    return f / 2 if w.causal else f
+
+
+def pass_flops(w: inputs.Workload, gemms: int) -> float:
+    """Flops of a kernel that runs `gemms` of the backward's N x M x D
+    contractions (the query pass runs 3: S, dP, dQ; the key pass 4: S, dP,
+    dV, dK), halved for a causal mask."""
+    f = 2.0 * gemms * w.B * w.H * w.N * w.M * w.DK
     return f / 2 if w.causal else f
 
 
@@ -226,10 +239,29 @@ def run_fab(args, rank, world, local):
 
     ws, packed = binding.alloc_backward(dims, dt, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    tensor_core = w.dtype == "bf16" and w.DK == w.DV and w.DK in (64, 128)
+
+    # the two launches of one backward step (what fab_backward enqueues)
+    if tensor_core:
+        stage_names = ("query_pass", "key_pass")
+
+        def first():
+            binding.fab_backward_query_pass(q, k, v, d, o, lse, mask, w.causal, w.scale, ws, packed)
+
+        def second():
+            binding.fab_backward_key_pass(q, k, v, d, lse, mask, w.causal, w.scale, ws, packed)
+    else:
+        stage_names = ("preprocess", "main")
+
+        def first():
+            binding.fab_backward_preprocess(d, o, dims, ws, packed)
+
+        def second():
+            binding.fab_backward_main(q, k, v, d, lse, mask, w.causal, w.scale, ws, packed)
 
     def step():
-        binding.fab_backward_preprocess(d, o, dims, ws, packed)
-        binding.fab_backward_main(q, k, v, d, lse, mask, w.causal, w.scale, ws, packed)
+        first()
+        second()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -249,9 +281,9 @@ def run_fab(args, rank, world, local):
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
-        binding.fab_backward_preprocess(d, o, dims, ws, packed)
+        first()
         ev[i][1].record(stream)
-        binding.fab_backward_main(q, k, v, d, lse, mask, w.causal, w.scale, ws, packed)
+        second()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -261,8 +293,8 @@ def run_fab(args, rank, world, local):
     if status != binding.FAB_OK:
         raise RuntimeError(f"device error in the timed region: {binding.status_string(status)}")
     step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    main_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    first_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    second_ms = [e[1].elapsed_time(e[2]) for e in ev]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world)
     flops = backward_flops(w)
@@ -347,14 +379,21 @@ def run_fab(args, rank, world, local):
             raise RuntimeError(f"device error in the e2e region: {binding.status_string(status)}")
 
     peaks, peak_src = load_peaks()
-    tensor_core = w.dtype == "bf16" and w.DK == w.DV and w.DK in (64, 128)
-    main_mean = statistics.mean(main_ms)
-    achieved = flops / (main_mean / 1e3) / 1e12
+    first_mean, second_mean = statistics.mean(first_ms), statistics.mean(second_ms)
     peak = float(peaks["bf16_tflops"])
+    if tensor_core:
+        # the dominant kernel of the two, with the contractions it runs itself
+        if second_mean >= first_mean:
+            kname, kms, kflops = "bwd_tc_kernel (key pass: S, dP, dV, dK)", second_mean, pass_flops(w, 4)
+        else:
+            kname, kms, kflops = "dq_tc_kernel (query pass: S, dP, dQ, D_i)", first_mean, pass_flops(w, 3)
+    else:
+        kname, kms, kflops = "dq_simt_kernel+dkdv_simt_kernel", second_mean, flops
+    achieved = kflops / (kms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": args.traffic_bytes if args.traffic_bytes is not None else MEASURED_TRAFFIC.get(w.name),
-                "kernel": "bwd_tc_kernel" if tensor_core else "dq_simt_kernel+dkdv_simt_kernel",
+                "kernel": kname, "kernel_ms": round(kms, 4), "kernel_flops": kflops,
                 "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone between L2 flushes)"}
 
     cpu = None
@@ -374,9 +413,9 @@ def run_fab(args, rank, world, local):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": 2 * args.steps,  # two kernels per step (see stages_ms)
             "clocks": clk,
-            "stages_ms": {"preprocess": round(statistics.mean(pre_ms), 4), "main": round(main_mean, 4)},
+            "stages_ms": {stage_names[0]: round(first_mean, 4), stage_names[1]: round(second_mean, 4)},
             "wall_s": round(wall, 4),
             "forward": ({"tflops": round(forward_flops(w) / (statistics.median(fwd_ms) / 1e3) / 1e12, 2),
                          "ms": round(statistics.median(fwd_ms), 3),

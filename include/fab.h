@@ -125,7 +125,9 @@ FAB_EXPORT int fab_forward_lse(const void* q, const void* k, const void* v, cons
  * fab_forward_lse on the same inputs.  d: device, `dtype`, [DV,H,N,B].
  * workspace: device, >= fab_backward_workspace_bytes() bytes, contents
  * overwritten.  packed_out: device f32, fab_packed_bytes() bytes, fully
- * overwritten (padding written as 0).  Enqueues fab_backward_preprocess then
+ * overwritten (padding written as 0).  Where the tensor-core kernels apply
+ * (bf16, DK == DV in {64, 128}) it enqueues fab_backward_query_pass then
+ * fab_backward_key_pass; otherwise fab_backward_preprocess then
  * fab_backward_main. */
 FAB_EXPORT int fab_backward(const void* q, const void* k, const void* v, const void* d, const void* o, const float* lse,
                  const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims, void* workspace,
@@ -143,6 +145,23 @@ FAB_EXPORT int fab_backward_preprocess(const void* d, const void* o, int dtype, 
 FAB_EXPORT int fab_backward_main(const void* q, const void* k, const void* v, const void* d, const float* lse,
                       const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims,
                       const void* workspace, size_t workspace_bytes, float* packed_out, fab_stream stream);
+
+/* The two tensor-core passes that make up fab_backward for bf16 inputs with
+ * DK == DV in {64, 128} (labml "Backward pass"); FAB_ERR_UNSUPPORTED
+ * otherwise.  Same arguments as fab_backward.
+ * fab_backward_query_pass: D_i = dO_i . O_i into the workspace, the dQ slice
+ * of packed_out (dQ_n = scale sum_m dS_nm K_m, recomputing S and dP per query
+ * tile) and the padding of packed_out.
+ * fab_backward_key_pass: the dK and dV slices of packed_out, reading D_i
+ * from the workspace (written by the query pass or fab_backward_preprocess);
+ * it does not read o. */
+FAB_EXPORT int fab_backward_query_pass(const void* q, const void* k, const void* v, const void* d, const void* o,
+                            const float* lse, const uint16_t* mask, int causal, float scale, int dtype,
+                            const fab_dims* dims, void* workspace, size_t workspace_bytes, float* packed_out,
+                            fab_stream stream);
+FAB_EXPORT int fab_backward_key_pass(const void* q, const void* k, const void* v, const void* d, const float* lse,
+                          const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims,
+                          const void* workspace, size_t workspace_bytes, float* packed_out, fab_stream stream);
 
 /* Largest B*H*N that fab_backward_noalloc accepts (query rows times heads
  * times batches): its fixed scratch holds one float per such row. */
