@@ -81,6 +81,32 @@ FAB_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_f
   }
 }
 
+// Waits until the shared-memory counter *c reaches `target` (acquire), with
+// the same abort and time-limit rules as mbar_wait.
+FAB_DEV bool counter_wait(const uint32_t* c, uint32_t target, volatile uint32_t* abort_flag, uint32_t* err) {
+  auto cur = [&]() {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(c)) : "memory");
+    return v;
+  };
+  if (cur() >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (cur() >= target) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1u;
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+// Adds one to the shared-memory counter *c (release).
+FAB_DEV void counter_bump(uint32_t* c) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(smem_u32(c)) : "memory");
+}
+
 // Bounded wait that ignores the abort flag; used while unwinding to let
 // in-flight asynchronous copies land before shared memory is released.
 FAB_DEV bool mbar_drain(uint32_t bar, uint32_t parity) {
@@ -120,6 +146,14 @@ FAB_DEV void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, 
 
 FAB_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
+// Waits until every bulk store this thread committed has finished reading
+// shared memory (the source may be overwritten; the global writes may still
+// be in flight).
+FAB_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// As bulk_wait_read_all, but only for all but the most recent group.
+FAB_DEV void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 // Waits until every bulk store this thread committed has completed (global
 // writes done, shared memory free).
 FAB_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -129,6 +163,22 @@ FAB_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "m
 FAB_DEV void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+
+// named_bar_sync that also returns the OR of `pred` over the participating
+// threads, so they all take the same branch afterwards.
+FAB_DEV bool named_bar_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+// Brings the 128-byte line holding `p` into L2.
+FAB_DEV void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 FAB_DEV void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -85,7 +85,7 @@ struct QCfg {
   static constexpr uint32_t ID_DQ = idesc_bf16(128, D, false, true);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_DQ + D <= TM_COLS, "tensor memory budget");
-  static_assert(OFF_Q == 0 && OFF_DO == TILE && D * 128 * 4 <= 2 * TILE, "dQ staging fits the Q and dO tiles");
+  static_assert(D * 128 * 4 == 2 * TILE, "dQ staging: one key stage per half of the columns");
 };
 
 enum : int {
@@ -97,10 +97,14 @@ enum : int {
   Q_DP = 14,      // + j % 3: dP(j) landed (value stage j % 2 free)
   Q_PD = 17,      // + j % 3: softmax warps read S(j) (its buffer is free)
   Q_DS = 20,      // + j % 3: softmax warps wrote dS(j)
-  Q_FINAL = 23,   // every dQ MMA finished
+  Q_FINAL = 23,   // phase k: unit k's dQ MMAs finished
   Q_FIN_S = 24,   // every S MMA finished
   Q_FIN_P = 25,   // every dP MMA finished
-  Q_COUNT = 26
+  Q_FIN_Q = 26,   // every dQ MMA finished
+  Q_QOE = 27,     // phase k: unit k's S and dP MMAs finished and its D_i read dO (Q, dO free)
+  Q_DF = 28,      // phase k: unit k's epilogue read dQ from tensor memory
+  Q_STG = 29,     // phase k: unit k's dQ is staged in shared memory
+  Q_COUNT = 30
 };
 static_assert(Q_COUNT <= 32, "barrier area holds 32 slots");
 
@@ -130,30 +134,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
+  // staging stages released by the bulk stores: two per unit, stage
+  // (G + 2) % 3 first, then G % 3 (G = the unit's last tile)
+  uint32_t* epi_cnt = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 8);
   uint32_t* err = &g_err_dq;
 
   const int warp = (int)warp_id();
   const int lane = (int)lane_id();
 
-  // heavy (late) query tiles first under a causal mask; heads of one GQA
-  // group are adjacent so their key/value tiles are shared through L2
-  const int64_t q_tiles = (p.N + C::BQ - 1) / C::BQ;
-  const int64_t units = p.H * p.B;
-  const int64_t qi = blockIdx.x / units;
-  const int64_t unit = blockIdx.x % units;
-  const int64_t h = unit % p.H, b = unit / p.H;
-  const int64_t hkv = h / (p.H / p.Hkv);
-  const int64_t qt = p.causal ? q_tiles - 1 - qi : qi;
-  const int64_t n0 = qt * C::BQ;
-  int64_t n_kv = (p.M + C::BK - 1) / C::BK;
-  if (p.causal) {
-    const int64_t last = (n0 + C::BQ - 1) / C::BK + 1;  // key tiles holding some m <= n
-    if (last < n_kv) n_kv = last;
-  }
-  const int nkv = (int)n_kv;
+  // work units: (query tile, head, batch), heavy (late) query tiles first
+  // under a causal mask; heads of one GQA group are adjacent so their
+  // key/value tiles are shared through L2.  CTA c takes units c, c + grid, ...
+  // (32-bit index arithmetic: the host guarantees units, N, M < 2^31)
+  const int q_tiles = (int)((p.N + C::BQ - 1) / C::BQ);
+  const int hb = (int)(p.H * p.B);
+  const int n_units = q_tiles * hb;
+  const int H = (int)p.H, rk2 = (int)(p.H / p.Hkv), m_tiles = (int)((p.M + C::BK - 1) / C::BK);
+  struct Unit {
+    int64_t h, b, hkv, n0;
+    int nkv;
+  };
+  auto unit_of = [&](int u) {
+    Unit x;
+    const int qi = u / hb, rem = u - qi * hb;
+    const int b = rem / H, h = rem - b * H;
+    x.h = h;
+    x.b = b;
+    x.hkv = h / rk2;
+    const int qt = p.causal ? q_tiles - 1 - qi : qi;
+    x.n0 = (int64_t)qt * C::BQ;
+    int n_kv = m_tiles;
+    if (p.causal) {
+      const int last = (qt * C::BQ + C::BQ - 1) / C::BK + 1;  // key tiles holding some m <= n
+      if (last < n_kv) n_kv = last;
+    }
+    x.nkv = n_kv;  // >= 1: key tile 0 holds m = 0 <= n
+    return x;
+  };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
+    *epi_cnt = 0u;
     mbar_init(bar(Q_QF), 1);
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(bar(Q_KF + s), 1);
@@ -169,6 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(Q_FINAL), 1);
     mbar_init(bar(Q_FIN_S), 1);
     mbar_init(bar(Q_FIN_P), 1);
+    mbar_init(bar(Q_FIN_Q), 1);
+    mbar_init(bar(Q_QOE), 2 + kSoftmaxThreads);
+    mbar_init(bar(Q_DF), kSoftmaxThreads);
+    mbar_init(bar(Q_STG), kSoftmaxThreads);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -182,37 +207,75 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && nkv > 0) {
+    // Per unit: V_0, K_0, then Q and dO (as soon as the previous unit's S and
+    // dP products and its D_i no longer need theirs), then V_j, K_j.  Stages
+    // and barrier phases count tiles g across units.  A unit's epilogue
+    // stages dQ in the key stages of its last two tiles G - 1 and G (the
+    // stages K(G+2) and K(G+3) would take), so those two loads also wait
+    // for that unit's stores to have read them.
+    if (lane == 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       prefetch_tensormap(&tmO);
-      mbar_arrive_expect_tx(bar(Q_QF), 2 * C::TILE);
-      for (int a = 0; a < C::ATOMS; ++a) {
-        tma_load_3d(sbase + C::OFF_Q + a * C::ATOM, &tmQ, bar(Q_QF), a * 64, (int)n0, (int)(b * p.H + h));
-        tma_load_4d(sbase + C::OFF_DO + a * C::ATOM, &tmO, bar(Q_QF), a * 64, (int)h, (int)n0, (int)b);
-      }
-      const int kvrow = (int)(b * p.Hkv + hkv);
-      int k_issued = 0, v_issued = 0;
       static_assert(C::KST == 3 && C::VST == 2, "stage recycling follows the three score buffers");
-      for (int j = 0; j < nkv; ++j) {
-        // value stage j % 2 held V(j-2): free once dP(j-2) finished
-        if (j >= 2 && !mbar_wait(bar(Q_DP + (j - 2) % 3), ((j - 2) / 3) & 1, abort_flag, err)) break;
-        const int vs = j % C::VST;
-        mbar_arrive_expect_tx(bar(Q_VF + vs), C::TILE);
-        for (int a = 0; a < C::ATOMS; ++a)
-          tma_load_3d(sbase + C::OFF_V + vs * C::TILE + a * C::ATOM, &tmV, bar(Q_VF + vs), a * 64, j * C::BK, kvrow);
-        ++v_issued;
-        // key stage j % 3 held K(j-3): free once dQ(j-3) finished
-        if (j >= 3 && !mbar_wait(bar(Q_KE + j % 3), ((j - 3) / 3) & 1, abort_flag, err)) break;
-        const int ks = j % C::KST;
-        mbar_arrive_expect_tx(bar(Q_KF + ks), C::TILE);
-        for (int a = 0; a < C::ATOMS; ++a)
-          tma_load_3d(sbase + C::OFF_K + ks * C::TILE + a * C::ATOM, &tmK, bar(Q_KF + ks), a * 64, j * C::BK, kvrow);
-        ++k_issued;
+      int g = 0, k = 0, k_issued = 0, v_issued = 0, qo_issued = 0;
+      int stG[3] = {-8, -8, -8}, stK[3] = {0, 0, 0};  // last tile and index of the latest units
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++k) {
+        const Unit x = unit_of(u);
+        const int kvrow = (int)(x.b * p.Hkv + x.hkv);
+        auto load_qo = [&]() {
+          if (k > 0 && !(ok = mbar_wait(bar(Q_QOE), (k - 1) & 1, abort_flag, err))) return;
+          mbar_arrive_expect_tx(bar(Q_QF), 2 * C::TILE);
+          for (int a = 0; a < C::ATOMS; ++a) {
+            tma_load_3d(sbase + C::OFF_Q + a * C::ATOM, &tmQ, bar(Q_QF), a * 64, (int)x.n0, (int)(x.b * p.H + x.h));
+            tma_load_4d(sbase + C::OFF_DO + a * C::ATOM, &tmO, bar(Q_QF), a * 64, (int)x.h, (int)x.n0, (int)x.b);
+          }
+          ++qo_issued;
+        };
+        bool qo = false;
+        for (int j = 0; j < x.nkv; ++j, ++g) {
+          if (j == 1) {
+            load_qo();
+            qo = true;
+            if (!ok) break;
+          }
+          // value stage g % 2 held V(g-2): free once dP(g-2) finished
+          if (g >= 2 && !(ok = mbar_wait(bar(Q_DP + (g - 2) % 3), ((g - 2) / 3) & 1, abort_flag, err))) break;
+          const int vs = g % C::VST;
+          mbar_arrive_expect_tx(bar(Q_VF + vs), C::TILE);
+          for (int a = 0; a < C::ATOMS; ++a)
+            tma_load_3d(sbase + C::OFF_V + vs * C::TILE + a * C::ATOM, &tmV, bar(Q_VF + vs), a * 64, j * C::BK,
+                        kvrow);
+          ++v_issued;
+          // key stage g % 3 held K(g-3): free once dQ(g-3) finished, and
+          // once any epilogue staging there has been stored
+          if (g >= 3 && !(ok = mbar_wait(bar(Q_KE + g % 3), ((g - 3) / 3) & 1, abort_flag, err))) break;
+          int need = 0;  // releases of staging stages this load must see
+#pragma unroll
+          for (int i = 0; i < 3; ++i)
+            if (stG[i] + 2 <= g && g <= stG[i] + 3) {
+              const int r2 = 2 * stK[i] + (g - stG[i] - 1);  // 2k+1 for K(G+2), 2k+2 for K(G+3)
+              if (r2 > need) need = r2;
+            }
+          if (need > 0) {
+            if (!(ok = counter_wait(epi_cnt, (uint32_t)need, abort_flag, err))) break;
+            fence_proxy_async_smem();
+          }
+          const int ks = g % C::KST;
+          mbar_arrive_expect_tx(bar(Q_KF + ks), C::TILE);
+          for (int a = 0; a < C::ATOMS; ++a)
+            tma_load_3d(sbase + C::OFF_K + ks * C::TILE + a * C::ATOM, &tmK, bar(Q_KF + ks), a * 64, j * C::BK,
+                        kvrow);
+          ++k_issued;
+        }
+        if (ok && !qo) load_qo();
+        stG[k % 3] = g - 1;
+        stK[k % 3] = k;
       }
       // let every load started above land before shared memory goes away
-      mbar_drain(bar(Q_QF), 0);
+      if (qo_issued > 0) mbar_drain(bar(Q_QF), (qo_issued - 1) & 1);
       for (int j = k_issued > C::KST ? k_issued - C::KST : 0; j < k_issued; ++j)
         mbar_drain(bar(Q_KF + j % C::KST), (j / C::KST) & 1);
       for (int j = v_issued > C::VST ? v_issued - C::VST : 0; j < v_issued; ++j)
@@ -220,247 +283,341 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 || warp >= 10) {
     // ------------------------------------------------------------ MMA issuers
-    // each issuer warp runs its loop convergently (descriptors stay
+    // each issuer warp runs its loops convergently (descriptors stay
     // warp-uniform); lane 0 issues the MMAs and commits
-    if (nkv > 0) {
-      const uint32_t issue = lane == 0 ? 1u : 0u;
-      auto wall = [&](int i, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, err));
-      };
-      // a K step only moves the descriptor's start address (address >> 4 in
-      // the low 14 bits, all addresses < 232 KB), so a step is one add
-      auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
-      auto kstep = [](int kk) { return (uint32_t)((kk >> 2) * C::ATOM + (kk & 3) * 32); };
-      auto buf = [](int x) { return (uint32_t)(x % 3) * C::TM_BUF; };
-      bool ok = wall(Q_QF, 0);
-      if (warp == 1) {
-        // S(j) = Q K_j^T into buffer j, which held dS(j-2)
-        const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
-        const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);  // key stage 0, K-major
-        for (int j = 0; ok && j < nkv; ++j) {
-          if (j >= 2 && !(ok = wall(Q_KE + (j - 2) % 3, ((j - 2) / 3) & 1))) break;
-          if (!(ok = wall(Q_KF + j % C::KST, (j / C::KST) & 1))) break;
+    const uint32_t issue = lane == 0 ? 1u : 0u;
+    auto wall = [&](int i, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, err));
+    };
+    // a K step only moves the descriptor's start address (address >> 4 in
+    // the low 14 bits, all addresses < 232 KB), so a step is one add
+    auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
+    auto kstep = [](int kk) { return (uint32_t)((kk >> 2) * C::ATOM + (kk & 3) * 32); };
+    auto buf = [](int x) { return (uint32_t)(x % 3) * C::TM_BUF; };
+    bool ok = true;
+    int g = 0, k = 0;
+    if (warp == 1) {
+      // S(g) = Q K^T into buffer g, which held dS(g-2)
+      const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);  // key stage 0, K-major
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++k) {
+        const int nkv = unit_of(u).nkv;
+        if (!(ok = wall(Q_QF, k & 1))) break;
+        for (int j = 0; j < nkv; ++j, ++g) {
+          if (g >= 2 && !(ok = wall(Q_KE + (g - 2) % 3, ((g - 2) / 3) & 1))) break;
+          if (!(ok = wall(Q_KF + g % C::KST, (g / C::KST) & 1))) break;
           tc_fence_after();
-          const uint64_t kd = adv(dK_km, (j % C::KST) * C::TILE);
+          const uint64_t kd = adv(dK_km, (g % C::KST) * C::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tm + buf(j), adv(dQ_km, kstep(kk)), adv(kd, kstep(kk)), C::ID_S, kk > 0, issue);
-          mma_commit(bar(Q_S + j % 3), issue);
+            mma_ss(tm + buf(g), adv(dQ_km, kstep(kk)), adv(kd, kstep(kk)), C::ID_S, kk > 0, issue);
+          mma_commit(bar(Q_S + g % 3), issue);
         }
-        mma_commit(bar(Q_FIN_S), issue);
-        mbar_drain(bar(Q_FIN_S), 0);
-      } else if (warp == 10) {
-        // dP(j) = dO V_j^T into buffer j + 2, which held S(j-1)
-        const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
-        const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
-        for (int j = 0; ok && j < nkv; ++j) {
-          if (j >= 1 && !(ok = wall(Q_PD + (j - 1) % 3, ((j - 1) / 3) & 1))) break;
-          if (!(ok = wall(Q_VF + j % C::VST, (j / C::VST) & 1))) break;
+        mma_commit(bar(Q_QOE), issue);  // the unit's S products are done with Q
+      }
+      mma_commit(bar(Q_FIN_S), issue);
+      mbar_drain(bar(Q_FIN_S), 0);
+    } else if (warp == 10) {
+      // dP(g) = dO V^T into buffer g + 2, which held S(g-1)
+      const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+      const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++k) {
+        const int nkv = unit_of(u).nkv;
+        if (!(ok = wall(Q_QF, k & 1))) break;
+        for (int j = 0; j < nkv; ++j, ++g) {
+          if (g >= 1 && !(ok = wall(Q_PD + (g - 1) % 3, ((g - 1) / 3) & 1))) break;
+          if (!(ok = wall(Q_VF + g % C::VST, (g / C::VST) & 1))) break;
           tc_fence_after();
-          const uint64_t vd = adv(dV_km, (j % C::VST) * C::TILE);
+          const uint64_t vd = adv(dV_km, (g % C::VST) * C::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tm + buf(j + 2), adv(dO_km, kstep(kk)), adv(vd, kstep(kk)), C::ID_S, kk > 0, issue);
-          mma_commit(bar(Q_DP + j % 3), issue);
+            mma_ss(tm + buf(g + 2), adv(dO_km, kstep(kk)), adv(vd, kstep(kk)), C::ID_S, kk > 0, issue);
+          mma_commit(bar(Q_DP + g % 3), issue);
         }
-        mma_commit(bar(Q_FIN_P), issue);
-        mbar_drain(bar(Q_FIN_P), 0);
-      } else if (warp == 11) {
-        // dQ += dS(j) K_j, dS(j) in buffer j + 2 (packed bf16: keys 0-63 at
-        // +0..31, keys 64-127 at +64..95), K_j MN-major
-        const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::ATOM, 1024);
-        auto a_col = [](int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); };
-        for (int j = 0; ok && j < nkv; ++j) {
-          if (!(ok = wall(Q_DS + j % 3, (j / 3) & 1))) break;
+        mma_commit(bar(Q_QOE), issue);  // the unit's dP products are done with dO
+      }
+      mma_commit(bar(Q_FIN_P), issue);
+      mbar_drain(bar(Q_FIN_P), 0);
+    } else if (warp == 11) {
+      // dQ += dS(g) K, dS(g) in buffer g + 2 (packed bf16: keys 0-63 at
+      // +0..31, keys 64-127 at +64..95), K MN-major; a unit's first product
+      // waits for the previous unit's epilogue to have read dQ
+      const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::ATOM, 1024);
+      auto a_col = [](int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); };
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++k) {
+        const int nkv = unit_of(u).nkv;
+        for (int j = 0; j < nkv; ++j, ++g) {
+          if (!(ok = wall(Q_DS + g % 3, (g / 3) & 1))) break;
+          if (j == 0 && k > 0 && !(ok = wall(Q_DF, (k - 1) & 1))) break;
           tc_fence_after();
-          const uint64_t kmn = adv(dK_mn, (j % C::KST) * C::TILE);
+          const uint64_t kmn = adv(dK_mn, (g % C::KST) * C::TILE);
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
-            mma_ts(tm + C::TM_DQ, tm + buf(j + 2) + a_col(kk), adv(kmn, kk * 2048), C::ID_DQ,
+            mma_ts(tm + C::TM_DQ, tm + buf(g + 2) + a_col(kk), adv(kmn, kk * 2048), C::ID_DQ,
                    (j > 0 || kk > 0) ? 1u : 0u, issue);
-          mma_commit(bar(Q_KE + j % 3), issue);
+          mma_commit(bar(Q_KE + g % 3), issue);
         }
-        // every dQ MMA (the last depends on every S and dP MMA) must finish
-        // before the epilogue reads dQ and tensor memory is released
+        // the unit's dQ (its last product depends on every S and dP MMA of
+        // the unit) is complete for the epilogue
         mma_commit(bar(Q_FINAL), issue);
-        mbar_drain(bar(Q_FINAL), 0);
+        if (!ok) break;
+        // the epilogue's bulk stores: once the softmax warps staged dQ, write
+        // it out and release the two staging stages as each has been read
+        if (!(ok = wall(Q_STG, k & 1))) break;
+        if (lane == 0) {
+          const Unit x = unit_of(u);
+          const int G = g - 1;
+          const uint32_t st0 = sbase + C::OFF_K + (uint32_t)((G + 2) % 3) * C::TILE;  // columns 0 .. D/2-1
+          const uint32_t st1 = sbase + C::OFF_K + (uint32_t)(G % 3) * C::TILE;        // columns D/2 .. D-1
+          for (int a = 0; a < D / 64; ++a)
+            tma_store_3d(&tmDQ, st0 + a * C::ATOM, a * 32, (int)x.n0, (int)(x.b * p.H + x.h));
+          bulk_commit_group();
+          for (int a = 0; a < D / 64; ++a)
+            tma_store_3d(&tmDQ, st1 + a * C::ATOM, D / 2 + a * 32, (int)x.n0, (int)(x.b * p.H + x.h));
+          bulk_commit_group();
+          bulk_wait_read_1();
+          counter_bump(epi_cnt);
+          bulk_wait_read_all();
+          counter_bump(epi_cnt);
+        }
+        __syncwarp();
       }
+      if (lane == 0) bulk_wait_all();
+      mma_commit(bar(Q_FIN_Q), issue);
+      mbar_drain(bar(Q_FIN_Q), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax / dS
     const int hf = (warp - 2) >> 2;        // warps 2-5: keys 0-63 of a tile, warps 6-9: keys 64-127
     const int r = (warp & 3) * 32 + lane;  // query row within the tile
-    const int64_t n = n0 + r;
-    const bool row_ok = n < p.N;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c1 = p.scale * kLog2e;
-    const int64_t rowidx = (b * p.H + h) * p.N + (row_ok ? n : 0);
-    // a row past N (zero-filled Q, dO) gets LSE = +inf, hence P = 0 and dS = 0
-    const float lse2 = row_ok ? p.lse[rowidx] * kLog2e : INFINITY;
-    float di;
-    if (FUSE_D) {
-      // D_i = dO_i . O_i: this thread takes columns hf * D/2 .. hf * D/2 + D/2 - 1
-      // of its row (O from global, dO from the swizzled tile in shared memory);
-      // the two halves meet in shared memory
-      uint4 ov[D / 16];
-      const uint4* orow = reinterpret_cast<const uint4*>(p.o + ((b * p.N + (row_ok ? n : 0)) * p.H + h) * D + hf * (D / 2));
-#pragma unroll
-      for (int c = 0; c < D / 16; ++c) ov[c] = row_ok ? __ldg(orow + c) : make_uint4(0, 0, 0, 0);
-      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(Q_QF), 0, abort_flag, err));
-      float part = 0.f;
-      if (got) {
-        auto dot2 = [](uint32_t a, uint32_t b) {
-          return __uint_as_float(a << 16) * __uint_as_float(b << 16) +
-                 __uint_as_float(a & 0xffff0000u) * __uint_as_float(b & 0xffff0000u);
-        };
-#pragma unroll
-        for (int c = 0; c < D / 16; ++c) {
-          const int e = hf * (D / 2) + 8 * c;  // first column of the 16-byte chunk
-          const uint4 dv = ld_shared_v4(sbase + C::OFF_DO + (uint32_t)(e / 64) * C::ATOM + r * 128 +
-                                        ((((e % 64) / 8) ^ (r & 7)) << 4));
-          part += dot2(dv.x, ov[c].x) + dot2(dv.y, ov[c].y) + dot2(dv.z, ov[c].z) + dot2(dv.w, ov[c].w);
-        }
-      }
-      float* dpart = reinterpret_cast<float*>(smem + C::OFF_DPART);
-      dpart[hf * C::BQ + r] = part;
-      named_bar_sync(2, kSoftmaxThreads);
-      di = dpart[r] + dpart[C::BQ + r];
-      if (hf == 0 && row_ok) p.di[rowidx] = di;
-      if (blockIdx.x == 0 && warp == 2 && lane == 0)
-#pragma unroll
-        for (int k = 0; k < 3; ++k)
-          for (int i = 0; i < p.pad_n[k]; ++i) p.pad[k][i] = 0.f;
-    } else {
-      di = row_ok ? p.di[rowidx] : 0.f;
-    }
-    // additive mask: this thread's 64 values (its query row, its 64 keys) of
-    // the next tile are loaded one tile ahead, as f16 pairs.  Entries past M
-    // read as 0; those keys are masked by the key bound anyway.
     const bool has_mask = p.mask != nullptr;
-    const uint16_t* mrow = p.mask + p.M * (row_ok ? n : 0);
-    const bool mvec = (p.M & 7) == 0;  // rows start 16-byte aligned
+    const bool mvec = (p.M & 7) == 0;  // mask rows start 16-byte aligned
+    float* dpart = reinterpret_cast<float*>(smem + C::OFF_DPART);
+    if (FUSE_D && blockIdx.x == 0 && warp == 2 && lane == 0)
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        for (int i = 0; i < p.pad_n[k]; ++i) p.pad[k][i] = 0.f;
+    // A unit's first global reads (this thread's LSE, its half row of O for
+    // D_i, its first mask chunk) are issued before the previous unit's
+    // epilogue, so their latency hides behind it.
+    uint4 ov[D / 16];
+    float lse_next = 0.f;
     uint32_t mk[32];
-    auto load_mask = [&](int jx) {
-      const int64_t mb = (int64_t)jx * C::BK + hf * 64;
-      if (!row_ok) {
+    auto fetch = [&](int uu) {
+      const Unit y = unit_of(uu);
+      const int64_t ny = y.n0 + r;
+      const bool ok_y = ny < p.N;
+      const int64_t ri = (y.b * p.H + y.h) * p.N + (ok_y ? ny : 0);
+      lse_next = ok_y ? __ldg(p.lse + ri) : 0.f;
+      if (FUSE_D) {
+        const uint4* orow =
+            reinterpret_cast<const uint4*>(p.o + ((y.b * p.N + (ok_y ? ny : 0)) * p.H + y.h) * D + hf * (D / 2));
 #pragma unroll
-        for (int c = 0; c < 32; ++c) mk[c] = 0u;
-      } else if (mvec && mb + 64 <= p.M) {
-        const uint4* src = reinterpret_cast<const uint4*>(mrow + mb);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = __ldg(src + c);
-          mk[4 * c] = v.x;
-          mk[4 * c + 1] = v.y;
-          mk[4 * c + 2] = v.z;
-          mk[4 * c + 3] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const uint32_t lo = (mb + 2 * c < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c) : 0u;
-          const uint32_t hi = (mb + 2 * c + 1 < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c + 1) : 0u;
-          mk[c] = lo | (hi << 16);
-        }
+        for (int c = 0; c < D / 16; ++c) ov[c] = ok_y ? __ldg(orow + c) : make_uint4(0, 0, 0, 0);
       }
     };
-    if (has_mask && nkv > 0) load_mask(0);
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const uint32_t sb = (uint32_t)(j % 3) * C::TM_BUF, db = (uint32_t)((j + 2) % 3) * C::TM_BUF;
-      const uint32_t ph = (uint32_t)(j / 3) & 1u;
-      const int64_t m0 = (int64_t)j * C::BK;
-      const int64_t mb = m0 + hf * 64;  // first key of this thread's columns
-      ok = mbar_wait(bar(Q_S + j % 3), ph, abort_flag, err);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      uint32_t ra[32], rb[32];
-      tmem_ld32(tm + lane_off + sb + hf * 64, ra);
-      tmem_ld32(tm + lane_off + sb + hf * 64 + 32, rb);
-      tmem_ld_wait2(ra, rb);
-      // S(j) is in registers: its buffer may take dP(j+1)
-      tc_fence_before();
-      mbar_arrive(bar(Q_PD + j % 3));
-      float pv[64];
+    int g = 0, k = 0;
+    if (blockIdx.x < n_units) fetch(blockIdx.x);
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
+      const Unit x = unit_of(u);
+      const int64_t n = x.n0 + r;
+      const bool row_ok = n < p.N;
+      const int64_t rowidx = (x.b * p.H + x.h) * p.N + (row_ok ? n : 0);
+      // a row past N (zero-filled Q, dO) gets LSE = +inf, hence P = 0 and dS = 0
+      const float lse2 = row_ok ? lse_next * kLog2e : INFINITY;
+      float di;
+      if (FUSE_D) {
+        // D_i = dO_i . O_i: this thread takes columns hf * D/2 .. hf * D/2 + D/2 - 1
+        // of its row (O fetched above, dO from the swizzled tile in shared
+        // memory); the two halves meet in shared memory
+        const bool got = __all_sync(0xffffffffu, mbar_wait(bar(Q_QF), k & 1, abort_flag, err));
+        float part = 0.f;
+        if (got) {
+          auto dot2 = [](uint32_t a, uint32_t b) {
+            return __uint_as_float(a << 16) * __uint_as_float(b << 16) +
+                   __uint_as_float(a & 0xffff0000u) * __uint_as_float(b & 0xffff0000u);
+          };
 #pragma unroll
-      for (int e = 0; e < 64; ++e) pv[e] = fmaf(__uint_as_float(e < 32 ? ra[e] : rb[e - 32]), c1, -lse2);
-      if (has_mask) {
+          for (int c = 0; c < D / 16; ++c) {
+            const int e = hf * (D / 2) + 8 * c;  // first column of the 16-byte chunk
+            const uint4 dv = ld_shared_v4(sbase + C::OFF_DO + (uint32_t)(e / 64) * C::ATOM + r * 128 +
+                                          ((((e % 64) / 8) ^ (r & 7)) << 4));
+            part += dot2(dv.x, ov[c].x) + dot2(dv.y, ov[c].y) + dot2(dv.z, ov[c].z) + dot2(dv.w, ov[c].w);
+          }
+        }
+        dpart[hf * C::BQ + r] = part;
+        named_bar_sync(2, kSoftmaxThreads);
+        di = dpart[r] + dpart[C::BQ + r];
+        if (hf == 0 && row_ok) p.di[rowidx] = di;
+      } else {
+        di = row_ok ? p.di[rowidx] : 0.f;
+      }
+      mbar_arrive(bar(Q_QOE));  // dO has been read for D_i
+      // additive mask: this thread's 64 values (its query row, its 64 keys) of
+      // the next tile are loaded one tile ahead, as f16 pairs.  Entries past M
+      // read as 0; those keys are masked by the key bound anyway.
+      const uint16_t* mrow = p.mask + p.M * (row_ok ? n : 0);
+      auto load_mask = [&](int jx) {
+        const int64_t mb = (int64_t)jx * C::BK + hf * 64;
+        if (!row_ok) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) mk[c] = 0u;
+        } else if (mvec && mb + 64 <= p.M) {
+          const uint4* src = reinterpret_cast<const uint4*>(mrow + mb);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = __ldg(src + c);
+            mk[4 * c] = v.x;
+            mk[4 * c + 1] = v.y;
+            mk[4 * c + 2] = v.z;
+            mk[4 * c + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t lo = (mb + 2 * c < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c) : 0u;
+            const uint32_t hi = (mb + 2 * c + 1 < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c + 1) : 0u;
+            mk[c] = lo | (hi << 16);
+          }
+        }
+      };
+      if (has_mask && k == 0) load_mask(0);  // later units: fetched with the previous unit's tail
+      bool ok = true;
+      int j = 0;
+      for (; j < x.nkv; ++j, ++g) {
+        const uint32_t sb = (uint32_t)(g % 3) * C::TM_BUF, db = (uint32_t)((g + 2) % 3) * C::TM_BUF;
+        const uint32_t ph = (uint32_t)(g / 3) & 1u;
+        const int64_t m0 = (int64_t)j * C::BK;
+        const int64_t mb = m0 + hf * 64;  // first key of this thread's columns
+        ok = mbar_wait(bar(Q_S + g % 3), ph, abort_flag, err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tm + lane_off + sb + hf * 64, ra);
+        tmem_ld32(tm + lane_off + sb + hf * 64 + 32, rb);
+        tmem_ld_wait2(ra, rb);
+        // S(g) is in registers: its buffer may take dP(g+1)
+        tc_fence_before();
+        mbar_arrive(bar(Q_PD + g % 3));
+        float pv[64];
+#pragma unroll
+        for (int e = 0; e < 64; ++e) pv[e] = fmaf(__uint_as_float(e < 32 ? ra[e] : rb[e - 32]), c1, -lse2);
+        if (has_mask) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mk[c]));
+            pv[2 * c] = fmaf(mf.x, kLog2e, pv[2 * c]);
+            pv[2 * c + 1] = fmaf(mf.y, kLog2e, pv[2 * c + 1]);
+          }
+          if (j + 1 < x.nkv) load_mask(j + 1);
+        }
+        // keys past the causal diagonal (top-left: key m > query n) or past M;
+        // only the diagonal tile and a ragged last tile have any
+        if ((p.causal && m0 + C::BK - 1 > x.n0) || m0 + C::BK > p.M) {
+          int64_t lim = 63;                              // last allowed column e (key mb + e)
+          if (p.causal && n - mb < lim) lim = n - mb;    // m <= n
+          if (p.M - 1 - mb < lim) lim = p.M - 1 - mb;    // m < M
+          const int li = lim < -1 ? -1 : (int)lim;
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e > li) pv[e] = -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < 64; ++e) pv[e] = ex2_approx(pv[e]);
+        ok = mbar_wait(bar(Q_DP + g % 3), ph, abort_flag, err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        tmem_ld32(tm + lane_off + db + hf * 64, ra);
+        tmem_ld32(tm + lane_off + db + hf * 64 + 32, rb);
+        tmem_ld_wait2(ra, rb);
+        uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mk[c]));
-          pv[2 * c] = fmaf(mf.x, kLog2e, pv[2 * c]);
-          pv[2 * c + 1] = fmaf(mf.y, kLog2e, pv[2 * c + 1]);
+          const int e = 2 * c;
+          const float d0 = __uint_as_float(e < 32 ? ra[e] : rb[e - 32]);
+          const float d1 = __uint_as_float(e + 1 < 32 ? ra[e + 1] : rb[e + 1 - 32]);
+          pk[c] = pack_bf16x2(pv[e] * (d0 - di), pv[e + 1] * (d1 - di));
         }
-        if (j + 1 < nkv) load_mask(j + 1);
+        // packed dS over the first 32 of this warp's own 64 dP columns (the
+        // other warp of the lane quarter reads only its own columns)
+        tmem_st32(tm + lane_off + db + hf * 64, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(Q_DS + g % 3));
       }
-      // keys past the causal diagonal (top-left: key m > query n) or past M;
-      // only the diagonal tile and a ragged last tile have any
-      if ((p.causal && m0 + C::BK - 1 > n0) || m0 + C::BK > p.M) {
-        int64_t lim = 63;                              // last allowed column e (key mb + e)
-        if (p.causal && n - mb < lim) lim = n - mb;    // m <= n
-        if (p.M - 1 - mb < lim) lim = p.M - 1 - mb;    // m < M
-        const int li = lim < -1 ? -1 : (int)lim;
+      g += x.nkv - j;  // keep the tile count in step after an early exit
+      if (u + (int)gridDim.x < n_units) {
+        fetch(u + gridDim.x);
+        if (has_mask) {
+          const Unit y = unit_of(u + gridDim.x);
+          const int64_t ny = y.n0 + r;
+          if (ny < p.N) {
+            const uint16_t* src = p.mask + p.M * ny + hf * 64;
+            if (mvec && hf * 64 + 64 <= p.M) {
+              const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
-          if (e > li) pv[e] = -INFINITY;
+              for (int c = 0; c < 8; ++c) {
+                const uint4 v = __ldg(s4 + c);
+                mk[4 * c] = v.x;
+                mk[4 * c + 1] = v.y;
+                mk[4 * c + 2] = v.z;
+                mk[4 * c + 3] = v.w;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const uint32_t lo = (hf * 64 + 2 * c < p.M) ? (uint32_t)__ldg(src + 2 * c) : 0u;
+                const uint32_t hi = (hf * 64 + 2 * c + 1 < p.M) ? (uint32_t)__ldg(src + 2 * c + 1) : 0u;
+                mk[c] = lo | (hi << 16);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mk[c] = 0u;
+          }
+        }
       }
-#pragma unroll
-      for (int e = 0; e < 64; ++e) pv[e] = ex2_approx(pv[e]);
-      ok = mbar_wait(bar(Q_DP + j % 3), ph, abort_flag, err);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      tmem_ld32(tm + lane_off + db + hf * 64, ra);
-      tmem_ld32(tm + lane_off + db + hf * 64 + 32, rb);
-      tmem_ld_wait2(ra, rb);
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int e = 2 * c;
-        const float d0 = __uint_as_float(e < 32 ? ra[e] : rb[e - 32]);
-        const float d1 = __uint_as_float(e + 1 < 32 ? ra[e + 1] : rb[e + 1 - 32]);
-        pk[c] = pack_bf16x2(pv[e] * (d0 - di), pv[e + 1] * (d1 - di));
-      }
-      // packed dS over the first 32 of this warp's own 64 dP columns (the
-      // other warp of the lane quarter reads only its own columns)
-      tmem_st32(tm + lane_off + db + hf * 64, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(Q_DS + j % 3));
-    }
-    // epilogue: dQ of this query tile (scaled), half of the columns per
-    // warp, staged in the now idle Q/dO area as 32-column atoms of 128-byte
-    // swizzled rows, then written by bulk tensor stores (rows past N are
-    // clipped by the store).  The tensor-memory loads are warp collectives,
-    // so every lane runs them.
-    const bool done = nkv > 0 && mbar_wait(bar(Q_FINAL), 0, abort_flag, err);
-    const bool write = __all_sync(0xffffffffu, done && !*abort_flag);
-    if (write) {
-      tc_fence_after();
+      // epilogue: dQ of this query tile (scaled), half of the columns per
+      // warp.  Staged in the key stages of the unit's last two tiles (their
+      // products are done; the producer holds the next loads into them until
+      // the dQ issuer's bulk stores have read them): columns 0 .. D/2-1 in
+      // stage (G + 2) % 3, the rest in stage G % 3, as 32-column atoms of
+      // 128-byte swizzled rows.  The stores clip rows past N.  The
+      // tensor-memory loads are warp collectives, so every lane runs them.
+      const int G = g - 1;  // the unit's last tile
+      auto stage = [&](int half) {
+        return sbase + C::OFF_K + (uint32_t)((half == 0 ? G + 2 : G) % 3) * C::TILE;
+      };
+      const bool done = mbar_wait(bar(Q_FINAL), k & 1, abort_flag, err);
+      const bool write = __all_sync(0xffffffffu, done && !*abort_flag);
+      if (write) {
+        tc_fence_after();
 #pragma unroll 1
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
-        uint32_t rv[32];
-        tmem_ld32(tm + lane_off + C::TM_DQ + hf * (D / 2) + c0, rv);
-        tmem_ld_wait(rv);
-        const uint32_t row = sbase + C::OFF_Q + (uint32_t)((hf * (D / 2) + c0) / 32) * C::ATOM + r * 128;
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t rv[32];
+          tmem_ld32(tm + lane_off + C::TM_DQ + hf * (D / 2) + c0, rv);
+          tmem_ld_wait(rv);
+          const uint32_t row = stage(hf) + (uint32_t)(c0 / 32) * C::ATOM + r * 128;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          st_shared_v4(row + ((k ^ (r & 7)) << 4), __float_as_uint(p.scale * __uint_as_float(rv[4 * k])),
-                       __float_as_uint(p.scale * __uint_as_float(rv[4 * k + 1])),
-                       __float_as_uint(p.scale * __uint_as_float(rv[4 * k + 2])),
-                       __float_as_uint(p.scale * __uint_as_float(rv[4 * k + 3])));
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(row + ((q ^ (r & 7)) << 4), __float_as_uint(p.scale * __uint_as_float(rv[4 * q])),
+                         __float_as_uint(p.scale * __uint_as_float(rv[4 * q + 1])),
+                         __float_as_uint(p.scale * __uint_as_float(rv[4 * q + 2])),
+                         __float_as_uint(p.scale * __uint_as_float(rv[4 * q + 3])));
+        }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
-    } else if (nkv == 0 && row_ok) {
-      float* dst = p.dq + rowidx * D + hf * (D / 2);
-      for (int c = 0; c < D / 2; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      // dQ has been read: the next unit's first dQ product may overwrite it;
+      // and it is staged: the dQ issuer writes it out
+      tc_fence_before();
+      mbar_arrive(bar(Q_DF));
+      mbar_arrive(bar(Q_STG));
+      // every softmax thread takes the same branch below
+      if (named_bar_or(1, kSoftmaxThreads, !write || *abort_flag != 0u)) break;
     }
-    named_bar_sync(1, kSoftmaxThreads);
-    if (warp == 2 && lane == 0 && write) {
-      for (int a = 0; a < D / 32; ++a)
-        tma_store_3d(&tmDQ, sbase + C::OFF_Q + a * C::ATOM, a * 32, (int)n0, (int)(b * p.H + h));
-      bulk_commit_group();
-      bulk_wait_all();
-    }
+    if (warp == 2 && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -536,7 +693,12 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
     p.pad[2] = pr.packed + pr.off_v / 4 + nk;
     p.pad_n[2] = (int)((pr.end - pr.off_v) / 4 - nk);
   }
-  const int64_t grid = ((pr.N + C::BQ - 1) / C::BQ) * pr.H * pr.B;
+  // persistent: one CTA per SM (each owns the SM's tensor memory), walking units
+  const int64_t units = ((pr.N + C::BQ - 1) / C::BQ) * pr.H * pr.B;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  const int64_t grid = units < sms ? units : sms;
   cudaError_t err =
       cudaFuncSetAttribute(dq_tc_kernel<D, FUSE_D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;

@@ -193,6 +193,46 @@ def test_every_slice_written_over_garbage(D, causal, mask):
         assert rel_err(got, ref[key]) <= TOL["bf16"], key
 
 
+@pytest.mark.parametrize("D,causal,mask", [(128, True, "none"), (64, False, "random"), (128, False, "random")])
+def test_two_phase_api_matches_fab_backward(D, causal, mask):
+    # fab_backward_preprocess + fab_backward_main (D_i from the preprocess),
+    # fab_backward_query_pass + fab_backward_key_pass and fab_backward (D_i
+    # inside the query pass) must give the same gradients bit for bit: the
+    # arithmetic per element is the same
+    w = inputs.custom(2, 4, 2, 300, 260, D, D, causal=causal, mask=mask, seed=41 + D)
+    x = inputs.make(w)
+    dev = torch.device("cuda")
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o, lse = binding.forward(g["q"], g["k"], g["v"], g["mask"], w.causal, w.scale)
+    dims = binding.make_dims(*w.dims)
+    ws, a = binding.alloc_backward(dims, binding.dtype_code(g["q"]), dev)
+    a.fill_(float("nan"))
+    binding.fab_backward(g["q"], g["k"], g["v"], g["d"], o, lse, g["mask"], w.causal, w.scale, ws, a)
+    ws2, b = binding.alloc_backward(dims, binding.dtype_code(g["q"]), dev)
+    b.fill_(float("nan"))
+    binding.fab_backward_preprocess(g["d"], o, dims, ws2, b)
+    binding.fab_backward_main(g["q"], g["k"], g["v"], g["d"], lse, g["mask"], w.causal, w.scale, ws2, b)
+    ws3, c = binding.alloc_backward(dims, binding.dtype_code(g["q"]), dev)
+    c.fill_(float("nan"))
+    binding.fab_backward_query_pass(g["q"], g["k"], g["v"], g["d"], o, lse, g["mask"], w.causal, w.scale, ws3, c)
+    binding.fab_backward_key_pass(g["q"], g["k"], g["v"], g["d"], lse, g["mask"], w.causal, w.scale, ws3, c)
+    assert binding.fab_last_device_error() == binding.FAB_OK
+    n = w.B * w.H * w.N
+    di_a = ws[: 4 * n].view(torch.float32).cpu()
+    di_b = ws2[: 4 * n].view(torch.float32).cpu()
+    # D_i: same products, summed in a different order by the two kernels
+    torch.testing.assert_close(di_a, di_b, rtol=1e-5, atol=1e-5)
+    assert torch.equal(a, c)
+    ref = oracle_ref(w, x)
+    for packed in (a, b):
+        p = packed.double().cpu().numpy()
+        assert np.all(np.isfinite(p))
+        check_pads_zero(w, p)
+        dq, dk, dv = (t.double().cpu().numpy() for t in binding.unpack(packed, dims))
+        for key, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+            assert rel_err(got, ref[key]) <= TOL["bf16"], key
+
+
 def test_many_tiles_repeatable_d128():
     # many query tiles per key tile (GQA group of 4, non-causal) exercises the
     # double-buffered score tiles and the shared lane quarters; no gradient
