@@ -177,9 +177,6 @@ FAB_DEV bool named_bar_or(uint32_t id, uint32_t count, bool pred) {
   return r != 0;
 }
 
-// Brings the 128-byte line holding `p` into L2.
-FAB_DEV void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
-
 FAB_DEV void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -403,19 +403,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // D_i, its first mask chunk) are issued before the previous unit's
     // epilogue, so their latency hides behind it.
     uint4 ov[D / 16];
-    float lse_next = 0.f;
+    float lse_next = 0.f, di_next = 0.f;
     uint32_t mk[32];
+    // (loads only, from a valid row: nothing here consumes a loaded value,
+    // so the loads stay in flight; a row past N is masked where the values
+    // are used)
     auto fetch = [&](int uu) {
       const Unit y = unit_of(uu);
-      const int64_t ny = y.n0 + r;
-      const bool ok_y = ny < p.N;
-      const int64_t ri = (y.b * p.H + y.h) * p.N + (ok_y ? ny : 0);
-      lse_next = ok_y ? __ldg(p.lse + ri) : 0.f;
+      const int64_t ny = y.n0 + r < p.N ? y.n0 + r : p.N - 1;
+      lse_next = __ldg(p.lse + (y.b * p.H + y.h) * p.N + ny);
+      if (!FUSE_D) di_next = p.di[(y.b * p.H + y.h) * p.N + ny];
       if (FUSE_D) {
-        const uint4* orow =
-            reinterpret_cast<const uint4*>(p.o + ((y.b * p.N + (ok_y ? ny : 0)) * p.H + y.h) * D + hf * (D / 2));
+        const uint4* orow = reinterpret_cast<const uint4*>(p.o + ((y.b * p.N + ny) * p.H + y.h) * D + hf * (D / 2));
 #pragma unroll
-        for (int c = 0; c < D / 16; ++c) ov[c] = ok_y ? __ldg(orow + c) : make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < D / 16; ++c) ov[c] = __ldg(orow + c);
       }
     };
     int g = 0, k = 0;
@@ -447,12 +448,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             part += dot2(dv.x, ov[c].x) + dot2(dv.y, ov[c].y) + dot2(dv.z, ov[c].z) + dot2(dv.w, ov[c].w);
           }
         }
-        dpart[hf * C::BQ + r] = part;
+        dpart[hf * C::BQ + r] = row_ok ? part : 0.f;
         named_bar_sync(2, kSoftmaxThreads);
         di = dpart[r] + dpart[C::BQ + r];
         if (hf == 0 && row_ok) p.di[rowidx] = di;
       } else {
-        di = row_ok ? p.di[rowidx] : 0.f;
+        di = row_ok ? di_next : 0.f;
       }
       mbar_arrive(bar(Q_QOE));  // dO has been read for D_i
       // additive mask: this thread's 64 values (its query row, its 64 keys) of

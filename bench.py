@@ -39,10 +39,14 @@ METRIC = "attn-backward TFLOP/s (dQ,dK,dV) and fraction of GB300 dense BF16 peak
 DEFAULT_WORKLOAD = "gqa_causal_d128"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM read + write bytes of one launch of the dominant kernel from an ncu
-# capture (profiles/), keyed by workload; entries are removed when the kernel
-# changes after the capture.
-MEASURED_TRAFFIC = {}
+# DRAM read + write bytes of one launch of each tensor-core pass from an ncu
+# capture (profiles/query_pass_*.md, profiles/key_pass_*.md), keyed by
+# (workload, pass); entries are removed when the kernel changes after the
+# capture.
+MEASURED_TRAFFIC = {
+    ("gqa_causal_d128", "query"): 255634176 + 99291136,
+    ("gqa_causal_d128", "key"): 291489024 + 38272768,
+}
 
 
 def backward_flops(w: inputs.Workload) -> float:
@@ -384,15 +388,15 @@ def run_fab(args, rank, world, local):
     if tensor_core:
         # the dominant kernel of the two, with the contractions it runs itself
         if second_mean >= first_mean:
-            kname, kms, kflops = "bwd_tc_kernel (key pass: S, dP, dV, dK)", second_mean, pass_flops(w, 4)
+            kname, kms, kflops, kkey = "bwd_tc_kernel (key pass: S, dP, dV, dK)", second_mean, pass_flops(w, 4), "key"
         else:
-            kname, kms, kflops = "dq_tc_kernel (query pass: S, dP, dQ, D_i)", first_mean, pass_flops(w, 3)
+            kname, kms, kflops, kkey = "dq_tc_kernel (query pass: S, dP, dQ, D_i)", first_mean, pass_flops(w, 3), "query"
     else:
-        kname, kms, kflops = "dq_simt_kernel+dkdv_simt_kernel", second_mean, flops
+        kname, kms, kflops, kkey = "dq_simt_kernel+dkdv_simt_kernel", second_mean, flops, None
     achieved = kflops / (kms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": args.traffic_bytes if args.traffic_bytes is not None else MEASURED_TRAFFIC.get(w.name),
+                "traffic": args.traffic_bytes if args.traffic_bytes is not None else MEASURED_TRAFFIC.get((w.name, kkey)),
                 "kernel": kname, "kernel_ms": round(kms, 4), "kernel_flops": kflops,
                 "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone between L2 flushes)"}
 
