@@ -144,15 +144,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // work units: (query tile, head, batch), heavy (late) query tiles first
   // under a causal mask; heads of one GQA group are adjacent so their
-  // key/value tiles are shared through L2.  CTA c takes units c, c + grid, ...
+  // key/value tiles are shared through L2.  Round k of the G CTAs takes units
+  // k G .. k G + G - 1, CTA c the c-th of them on even rounds and the
+  // (G-1-c)-th on odd rounds, which evens out the per-CTA totals.
   // (32-bit index arithmetic: the host guarantees units, N, M < 2^31)
   const int q_tiles = (int)((p.N + C::BQ - 1) / C::BQ);
   const int hb = (int)(p.H * p.B);
   const int n_units = q_tiles * hb;
   const int H = (int)p.H, rk2 = (int)(p.H / p.Hkv), m_tiles = (int)((p.M + C::BK - 1) / C::BK);
   struct Unit {
-    int64_t h, b, hkv, n0;
-    int nkv;
+    int h, b, hkv, n0, nkv;  // 32-bit; products that can exceed 2^31 widen first
+  };
+  auto unit_at = [&](int kk) {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    return G * kk + ((kk & 1) ? G - 1 - c : c);
   };
   auto unit_of = [&](int u) {
     Unit x;
@@ -162,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.b = b;
     x.hkv = h / rk2;
     const int qt = p.causal ? q_tiles - 1 - qi : qi;
-    x.n0 = (int64_t)qt * C::BQ;
+    x.n0 = qt * C::BQ;
     int n_kv = m_tiles;
     if (p.causal) {
       const int last = (qt * C::BQ + C::BQ - 1) / C::BK + 1;  // key tiles holding some m <= n
@@ -222,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0, k = 0, k_issued = 0, v_issued = 0, qo_issued = 0;
       int stG[3] = {-8, -8, -8}, stK[3] = {0, 0, 0};  // last tile and index of the latest units
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++k) {
+      for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
         const Unit x = unit_of(u);
         const int kvrow = (int)(x.b * p.Hkv + x.hkv);
         auto load_qo = [&]() {
@@ -300,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S(g) = Q K^T into buffer g, which held dS(g-2)
       const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
       const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);  // key stage 0, K-major
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++k) {
+      for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
         const int nkv = unit_of(u).nkv;
         if (!(ok = wall(Q_QF, k & 1))) break;
         for (int j = 0; j < nkv; ++j, ++g) {
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dP(g) = dO V^T into buffer g + 2, which held S(g-1)
       const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
       const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++k) {
+      for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
         const int nkv = unit_of(u).nkv;
         if (!(ok = wall(Q_QF, k & 1))) break;
         for (int j = 0; j < nkv; ++j, ++g) {
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // waits for the previous unit's epilogue to have read dQ
       const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::ATOM, 1024);
       auto a_col = [](int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); };
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++k) {
+      for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
         const int nkv = unit_of(u).nkv;
         for (int j = 0; j < nkv; ++j, ++g) {
           if (!(ok = wall(Q_DS + g % 3, (g / 3) & 1))) break;
@@ -420,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     int g = 0, k = 0;
-    if (blockIdx.x < n_units) fetch(blockIdx.x);
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
+    if (unit_at(0) < n_units) fetch(unit_at(0));
+    for (int u = unit_at(0); u < n_units; u = unit_at(++k)) {
       const Unit x = unit_of(u);
       const int64_t n = x.n0 + r;
       const bool row_ok = n < p.N;
@@ -549,10 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(Q_DS + g % 3));
       }
       g += x.nkv - j;  // keep the tile count in step after an early exit
-      if (u + (int)gridDim.x < n_units) {
-        fetch(u + gridDim.x);
+      if (unit_at(k + 1) < n_units) {
+        fetch(unit_at(k + 1));
         if (has_mask) {
-          const Unit y = unit_of(u + gridDim.x);
+          const Unit y = unit_of(unit_at(k + 1));
           const int64_t ny = y.n0 + r;
           if (ny < p.N) {
             const uint16_t* src = p.mask + p.M * ny + hf * 64;
