@@ -46,7 +46,8 @@
 // The products are issued by two warps, each waiting only on its own inputs.
 // One issues dP^T(i) once S^T(i) was read, then S^T(i+1) once Q_{i+1} landed
 // and dV(i-1), dK(i-1) are done.  The other issues dV(i) + dK(i) once P^T(i),
-// dS^T(i) are written.  A single issuing thread stalls the tensor pipe for
+// dS^T(i) are written.  (Holding dV(i), dK(i) back until dP^T(i+1) is issued
+// was measured slower: it delays the buffer S^T(i+2) needs.)  A single issuing thread stalls the tensor pipe for
 // one to two hundred cycles at every commit and barrier wait; with two
 // streams those stalls overlap the other stream's MMAs.
 //
@@ -188,6 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_FINAL), 1);
     mbar_init(bar(B_FIN_S), 1);
     fence_mbar_init();
+    if (n_it > 0) {
+      // this thread is the producer's issuing lane: start the key/value tile
+      // copies before the tensor-memory allocation and block sync below
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmO);
+      mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
+      const int kvrow = (int)(b * p.Hkv + hkv);
+      for (int a = 0; a < C::ATOMS; ++a) {
+        tma_load_3d(sbase + C::OFF_K + a * C::ATOM, &tmK, bar(B_KV), a * 64, (int)m0, kvrow);
+        tma_load_3d(sbase + C::OFF_V + a * C::ATOM, &tmV, bar(B_KV), a * 64, (int)m0, kvrow);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), C::TM_COLS);
@@ -202,18 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     int issued = 0;
     if (n_it > 0) {
-      if (lane == 0) {
-        prefetch_tensormap(&tmQ);
-        prefetch_tensormap(&tmK);
-        prefetch_tensormap(&tmV);
-        prefetch_tensormap(&tmO);
-        mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
-        const int kvrow = (int)(b * p.Hkv + hkv);
-        for (int a = 0; a < C::ATOMS; ++a) {
-          tma_load_3d(sbase + C::OFF_K + a * C::ATOM, &tmK, bar(B_KV), a * 64, (int)m0, kvrow);
-          tma_load_3d(sbase + C::OFF_V + a * C::ATOM, &tmV, bar(B_KV), a * 64, (int)m0, kvrow);
-        }
-      }
+      // (the key/value tile copies were started at barrier initialisation)
       int q_issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int qs = it % C::QST, os = it % C::OST;
@@ -516,7 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_store_3d(&tmDK, sbase + C::OFF_STAGE + C::STAGE_DK + a * C::ATOM, a * 32, (int)m0, kvrow);
       }
       bulk_commit_group();
-      bulk_wait_all();
+      // the stores must have read shared memory before the CTA exits (their
+      // global writes complete before the grid does)
+      bulk_wait_read_all();
     }
   }
 

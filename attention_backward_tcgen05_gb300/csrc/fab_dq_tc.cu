@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      if (lane == 0) bulk_wait_all();
+      if (lane == 0) bulk_wait_read_all();  // (every group was waited for above; kept for an early exit)
       mma_commit(bar(Q_FIN_Q), issue);
       mbar_drain(bar(Q_FIN_Q), 0);
     }
@@ -416,12 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto fetch = [&](int uu) {
       const Unit y = unit_of(uu);
       const int64_t ny = y.n0 + r < p.N ? y.n0 + r : p.N - 1;
-      lse_next = __ldg(p.lse + (y.b * p.H + y.h) * p.N + ny);
+      lse_next = ld_global_nc_f32(p.lse + (y.b * p.H + y.h) * p.N + ny);
       if (!FUSE_D) di_next = p.di[(y.b * p.H + y.h) * p.N + ny];
       if (FUSE_D) {
         const uint4* orow = reinterpret_cast<const uint4*>(p.o + ((y.b * p.N + ny) * p.H + y.h) * D + hf * (D / 2));
 #pragma unroll
-        for (int c = 0; c < D / 16; ++c) ov[c] = __ldg(orow + c);
+        for (int c = 0; c < D / 16; ++c) ov[c] = ld_global_nc_v4(orow + c);
       }
     };
     int g = 0, k = 0;
@@ -623,7 +623,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every softmax thread takes the same branch below
       if (named_bar_or(1, kSoftmaxThreads, !write || *abort_flag != 0u)) break;
     }
-    if (warp == 2 && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
