@@ -104,7 +104,8 @@ enum : int {
   Q_QOE = 27,     // phase k: unit k's S and dP MMAs finished and its D_i read dO (Q, dO free)
   Q_DF = 28,      // phase k: unit k's epilogue read dQ from tensor memory
   Q_STG = 29,     // phase k: unit k's dQ is staged in shared memory
-  Q_COUNT = 30
+  Q_DQI = 30,     // phase k: unit k's last dQ products have been issued
+  Q_COUNT = 31
 };
 static_assert(Q_COUNT <= 32, "barrier area holds 32 slots");
 
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(Q_QOE), 2 + kSoftmaxThreads);
     mbar_init(bar(Q_DF), kSoftmaxThreads);
     mbar_init(bar(Q_STG), kSoftmaxThreads);
+    mbar_init(bar(Q_DQI), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -308,6 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
         const int nkv = unit_of(u).nkv;
         if (!(ok = wall(Q_QF, k & 1))) break;
+        // the previous unit's last dQ products go into the tensor pipe
+        // before this unit's first scores: its epilogue waits for them
+        if (k > 0 && !(ok = wall(Q_DQI, (k - 1) & 1))) break;
         for (int j = 0; j < nkv; ++j, ++g) {
           if (g >= 2 && !(ok = wall(Q_KE + (g - 2) % 3, ((g - 2) / 3) & 1))) break;
           if (!(ok = wall(Q_KF + g % C::KST, (g / C::KST) & 1))) break;
@@ -329,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
         const int nkv = unit_of(u).nkv;
         if (!(ok = wall(Q_QF, k & 1))) break;
+        if (k > 0 && !(ok = wall(Q_DQI, (k - 1) & 1))) break;  // as for the scores
         for (int j = 0; j < nkv; ++j, ++g) {
           if (g >= 1 && !(ok = wall(Q_PD + (g - 1) % 3, ((g - 1) / 3) & 1))) break;
           if (!(ok = wall(Q_VF + g % C::VST, (g / C::VST) & 1))) break;
@@ -365,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the unit's dQ (its last product depends on every S and dP MMA of
         // the unit) is complete for the epilogue
         mma_commit(bar(Q_FINAL), issue);
+        if (lane == 0) mbar_arrive(bar(Q_DQI));
         if (!ok) break;
         // the epilogue's bulk stores: once the softmax warps staged dQ, write
         // it out and release the two staging stages as each has been read
