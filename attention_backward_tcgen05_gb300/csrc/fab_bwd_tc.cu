@@ -93,9 +93,6 @@ struct Cfg {
   // (no room for alignment slack at D = 128); at least 116 KB so one CTA
   // owns an SM and its whole tensor memory
   static constexpr uint32_t SMEM_USED = OFF_MISC + 64;
-  // epilogue staging of dV and dK (f32, 32-column atoms), over the tiles
-  static constexpr uint32_t OFF_STAGE = 0;
-  static constexpr uint32_t STAGE_DK = (D / 32) * ATOM;
   static constexpr uint32_t SMEM = SMEM_USED > 118784 ? SMEM_USED : 118784;
   // tensor-memory columns: tile buffer b at 128 b (b = 0, 1)
   static constexpr uint32_t TM_X = 128, TM_DV = 256, TM_DK = 256 + D;
@@ -104,13 +101,16 @@ struct Cfg {
   static constexpr uint32_t ID_DVK = idesc_bf16(128, D, false, true);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_DK + D <= TM_COLS, "tensor memory budget");
-  static_assert(OFF_STAGE + 2 * STAGE_DK <= OFF_LD, "dV/dK staging fits the tile area");
+  // epilogue staging (f32, 32-column atoms): dV over the key and value
+  // tiles, dK over one Q and one dO stage
+  static_assert((D / 32) * ATOM == OFF_V + TILE - OFF_K, "dV staging fills the key/value tiles");
+  static_assert((D / 64) * ATOM == TILE, "each half of dK fills one ring stage");
   static_assert(QST <= 4 && OST <= QST, "barrier slots hold up to four stages; the dO ring is not deeper");
 };
 
 // barrier slots
 enum : int {
-  B_KV = 0,
+  B_KV = 0,       // phase k: unit k's key tile landed
   B_FQ = 1,       // + i % QST: Q_i landed
   B_FO = 5,       // + i % OST: dO_i, LSE and D rows of tile i landed
   B_XF = 9,       // + i % QST: dV(i), dK(i) finished (Q and dO stages of i, buffer i % 2 free)
@@ -118,9 +118,13 @@ enum : int {
   B_SF = 15,      // + i % 2: softmax warps read S^T(i)
   B_DP = 17,      // + i % 2: dP^T(i) landed
   B_DS = 19,      // + i % 2: softmax warps wrote P^T(i) and dS^T(i)
-  B_FINAL = 21,   // every dV/dK MMA finished
+  B_FINAL = 21,   // phase k: unit k's dV/dK MMAs finished
   B_FIN_S = 22,   // every S^T and dP^T MMA finished
-  B_COUNT = 23
+  B_FIN_X = 23,   // every dV/dK MMA finished
+  B_DF = 24,      // phase k: unit k's epilogue read dV, dK from tensor memory
+  B_STG = 25,     // phase k: unit k's dV, dK are staged in shared memory
+  B_V = 26,       // phase k: unit k's value tile landed
+  B_COUNT = 27
 };
 static_assert(B_COUNT <= 32, "barrier area holds 32 slots");
 
@@ -135,7 +139,7 @@ struct Params {
   float* dv;
 };
 
-template <int D>
+template <int D, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -153,28 +157,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
+  // units whose dV/dK staging the bulk stores have finished reading: the
+  // part in the key tile, the part in the value tile, the part in one Q and
+  // one dO stage (in that order)
+  uint32_t* k_cnt = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 8);
+  uint32_t* v_cnt = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 12);
+  uint32_t* r_cnt = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 16);
   float* ld_smem = reinterpret_cast<float*>(smem + C::OFF_LD);
   uint32_t* err = &g_err_tc;
 
   const int warp = (int)warp_id();
   const int lane = (int)lane_id();
 
-  // tile coordinates: heavy (low) key tiles first so a causal grid drains evenly
-  const int64_t units = p.Hkv * p.B;
-  const int64_t j = blockIdx.x / units;
-  const int64_t rem = blockIdx.x % units;
-  const int64_t b = rem / p.Hkv, hkv = rem % p.Hkv;
-  const int64_t m0 = j * C::BM;
-  const int64_t rk2 = p.H / p.Hkv;
-  const int64_t q_tiles = (p.N + C::BQ - 1) / C::BQ;
-  int64_t qt0 = p.causal ? m0 / C::BQ : 0;  // first query tile holding some n >= m0
-  if (qt0 > q_tiles) qt0 = q_tiles;
-  const int64_t nqt = q_tiles - qt0;
-  const int n_it = (int)(rk2 * nqt);
+  // work units: (key tile, key/value head, batch), heavy (low) key tiles
+  // first under a causal mask.  Round k of the G CTAs takes units k G ..
+  // k G + G - 1, CTA c the c-th of them on even rounds and the (G-1-c)-th on
+  // odd rounds.  (32-bit index arithmetic: the host guarantees units, N,
+  // M < 2^31.)  A unit with no query at or after its keys (causal, M > N)
+  // has n_it = 0: its dK, dV rows are zero.
+  const int hb = (int)(p.Hkv * p.B);
+  const int m_tiles = (int)((p.M + C::BM - 1) / C::BM);
+  const int n_units = m_tiles * hb;
+  const int rk2 = (int)(p.H / p.Hkv);
+  const int q_tiles = (int)((p.N + C::BQ - 1) / C::BQ);
+  struct Unit {
+    int b, hkv, m0, qt0, n_it;
+  };
+  auto unit_at = [&](int kk) {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    return G * kk + ((kk & 1) ? G - 1 - c : c);
+  };
+  auto unit_of = [&](int u) {
+    Unit x;
+    const int jt = u / hb, rem = u - jt * hb;
+    x.b = rem / (int)p.Hkv;
+    x.hkv = rem - x.b * (int)p.Hkv;
+    x.m0 = jt * C::BM;
+    int qt0 = p.causal ? x.m0 / C::BQ : 0;  // first query tile holding some n >= m0
+    if (qt0 > q_tiles) qt0 = q_tiles;
+    x.qt0 = qt0;
+    x.n_it = rk2 * (q_tiles - qt0);
+    return x;
+  };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
+    *k_cnt = 0u;
+    *v_cnt = 0u;
+    *r_cnt = 0u;
     mbar_init(bar(B_KV), 1);
+    mbar_init(bar(B_V), 1);
     for (int s = 0; s < C::QST; ++s) {
       mbar_init(bar(B_FQ + s), 1);
       mbar_init(bar(B_XF + s), 1);
@@ -188,20 +220,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_FINAL), 1);
     mbar_init(bar(B_FIN_S), 1);
+    mbar_init(bar(B_FIN_X), 1);
+    mbar_init(bar(B_DF), kSoftmaxThreads);
+    mbar_init(bar(B_STG), kSoftmaxThreads);
     fence_mbar_init();
-    if (n_it > 0) {
-      // this thread is the producer's issuing lane: start the key/value tile
-      // copies before the tensor-memory allocation and block sync below
-      prefetch_tensormap(&tmQ);
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-      prefetch_tensormap(&tmO);
-      mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
-      const int kvrow = (int)(b * p.Hkv + hkv);
+    // this thread is the producer's issuing lane: start the first unit's
+    // key/value tile copies before the tensor-memory allocation and block
+    // sync below
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    prefetch_tensormap(&tmO);
+    for (int kk = 0; unit_at(kk) < n_units; ++kk) {
+      const Unit x = unit_of(unit_at(kk));
+      if (x.n_it == 0) continue;
+      mbar_arrive_expect_tx(bar(B_KV), C::TILE);
+      mbar_arrive_expect_tx(bar(B_V), C::TILE);
+      const int kvrow = x.b * (int)p.Hkv + x.hkv;
       for (int a = 0; a < C::ATOMS; ++a) {
-        tma_load_3d(sbase + C::OFF_K + a * C::ATOM, &tmK, bar(B_KV), a * 64, (int)m0, kvrow);
-        tma_load_3d(sbase + C::OFF_V + a * C::ATOM, &tmV, bar(B_KV), a * 64, (int)m0, kvrow);
+        tma_load_3d(sbase + C::OFF_K + a * C::ATOM, &tmK, bar(B_KV), a * 64, x.m0, kvrow);
+        tma_load_3d(sbase + C::OFF_V + a * C::ATOM, &tmV, bar(B_V), a * 64, x.m0, kvrow);
       }
+      break;
     }
   }
   if (warp == 1) {
@@ -215,23 +255,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int issued = 0;
-    if (n_it > 0) {
-      // (the key/value tile copies were started at barrier initialisation)
-      int q_issued = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int qs = it % C::QST, os = it % C::OST;
-        const int64_t h = hkv * rk2 + it % rk2;
-        const int64_t n0 = (qt0 + it / rk2) * C::BQ;
-        const int64_t rowbase = (b * p.H + h) * p.N;
-        const int qrow = (int)(b * p.H + h);
-        // Q stage qs held tile it - QST: free once its dV and dK finished
-        bool ok = it < C::QST || mbar_wait(bar(B_XF + qs), ((it / C::QST) - 1) & 1, abort_flag, err);
+    // Per unit: an L2 prefetch of the next unit's key/value tiles, Q_g and
+    // dO_g (with the tile's LSE and D rows) for every tile g, the key/value
+    // tiles after the first tile's.  Stages and barrier phases count tiles g
+    // across units.  A unit's epilogue stages dV in the key and value tiles
+    // and dK in the Q and dO stages of its last tile G, so the next unit's
+    // key tile, value tile, Q_{G+QST} and dO_{G+OST} also wait for that
+    // unit's bulk stores to have read the part they overwrite.
+    int g = 0, ku = 0, q_issued = 0, o_issued = 0;
+    int kv_issued = 0;  // the first unit's copies were started at barrier initialisation
+    for (int kk = 0; kv_issued == 0 && unit_at(kk) < n_units; ++kk)
+      if (unit_of(unit_at(kk)).n_it > 0) kv_issued = 1;
+    int stG[3] = {-64, -64, -64}, stK[3] = {0, 0, 0};  // last tile and index of the latest units
+    bool ok = true;
+    // a load into the stage tile gg - dist left: wait for the staging of the
+    // unit (if any) whose last tile that was
+    auto staged_wait = [&](int gg, int dist) {
+#pragma unroll
+      for (int i = 0; i < 3; ++i)
+        if (stG[i] + dist == gg) return counter_wait(r_cnt, (uint32_t)(stK[i] + 1), abort_flag, err);
+      return true;
+    };
+    for (int kk = 0; ok && unit_at(kk) < n_units; ++kk) {
+      const Unit x = unit_of(unit_at(kk));
+      if (x.n_it == 0) continue;
+      if (lane == 0)
+        for (int k2 = kk + 1; unit_at(k2) < n_units; ++k2) {
+          const Unit y = unit_of(unit_at(k2));
+          if (y.n_it == 0) continue;
+          for (int a = 0; a < C::ATOMS; ++a) {
+            tma_prefetch_3d(&tmK, a * 64, y.m0, y.b * (int)p.Hkv + y.hkv);
+            tma_prefetch_3d(&tmV, a * 64, y.m0, y.b * (int)p.Hkv + y.hkv);
+          }
+          break;
+        }
+      for (int it = 0; it < x.n_it; ++it, ++g) {
+        const int qs = g % C::QST, os = g % C::OST;
+        const int h = x.hkv * rk2 + it % rk2;
+        const int n0 = (x.qt0 + it / rk2) * C::BQ;
+        const int64_t rowbase = ((int64_t)x.b * p.H + h) * p.N;
+        const int qrow = x.b * (int)p.H + h;
+        // Q stage qs held tile g - QST: free once its dV and dK finished
+        ok = (g < C::QST || mbar_wait(bar(B_XF + qs), ((g / C::QST) - 1) & 1, abort_flag, err)) &&
+             staged_wait(g, C::QST);
         if (!__all_sync(0xffffffffu, ok)) break;
+        fence_proxy_async_smem();
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(B_FQ + qs), C::TILE);
           for (int a = 0; a < C::ATOMS; ++a)
-            tma_load_3d(sbase + C::OFF_Q + qs * C::TILE + a * C::ATOM, &tmQ, bar(B_FQ + qs), a * 64, (int)n0, qrow);
+            tma_load_3d(sbase + C::OFF_Q + qs * C::TILE + a * C::ATOM, &tmQ, bar(B_FQ + qs), a * 64, n0, qrow);
         }
         ++q_issued;
         // the tile's LSE and D rows, into registers first: their latency
@@ -244,14 +316,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           lv[k] = in ? __ldg(p.lse + rowbase + n) * kLog2e : INFINITY;
           dv[k] = in ? __ldg(p.di + rowbase + n) : 0.f;
         }
-        // dO stage os held tile it - OST: free once its dV and dK finished
-        ok = it < C::OST || mbar_wait(bar(B_XF + (it - C::OST) % C::QST), ((it - C::OST) / C::QST) & 1, abort_flag, err);
+        // dO stage os held tile g - OST: free once its dV and dK finished
+        ok = (g < C::OST ||
+              mbar_wait(bar(B_XF + (g - C::OST) % C::QST), ((g - C::OST) / C::QST) & 1, abort_flag, err)) &&
+             staged_wait(g, C::OST);
         if (!__all_sync(0xffffffffu, ok)) break;
+        fence_proxy_async_smem();
         if (lane == 0) {
           mbar_expect_tx(bar(B_FO + os), C::TILE);
           for (int a = 0; a < C::ATOMS; ++a)
-            tma_load_4d(sbase + C::OFF_DO + os * C::TILE + a * C::ATOM, &tmO, bar(B_FO + os), a * 64, (int)h,
-                        (int)n0, (int)b);
+            tma_load_4d(sbase + C::OFF_DO + os * C::TILE + a * C::ATOM, &tmO, bar(B_FO + os), a * 64, h, n0, x.b);
         }
         float* lds = ld_smem + os * 2 * C::BQ;
 #pragma unroll
@@ -261,227 +335,329 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // one arrival per lane (count 32) publishes that lane's LSE/D stores
         mbar_arrive(bar(B_FO + os));
-        ++issued;
+        ++o_issued;
+        if (it == 0) {
+          // the unit's key and value tiles (the first unit's were started
+          // at barrier initialisation): the previous unit's dV staging there
+          // must have been read
+          if (ku > 0) {
+            const int kvrow = x.b * (int)p.Hkv + x.hkv;
+            ok = counter_wait(k_cnt, (uint32_t)ku, abort_flag, err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            fence_proxy_async_smem();
+            if (lane == 0) {
+              mbar_arrive_expect_tx(bar(B_KV), C::TILE);
+              for (int a = 0; a < C::ATOMS; ++a)
+                tma_load_3d(sbase + C::OFF_K + a * C::ATOM, &tmK, bar(B_KV), a * 64, x.m0, kvrow);
+            }
+            ok = counter_wait(v_cnt, (uint32_t)ku, abort_flag, err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            fence_proxy_async_smem();
+            if (lane == 0) {
+              mbar_arrive_expect_tx(bar(B_V), C::TILE);
+              for (int a = 0; a < C::ATOMS; ++a)
+                tma_load_3d(sbase + C::OFF_V + a * C::ATOM, &tmV, bar(B_V), a * 64, x.m0, kvrow);
+            }
+            ++kv_issued;
+          }
+        }
       }
-      // let every load this warp started land before shared memory goes away
-      if (lane == 0) {
-        mbar_drain(bar(B_KV), 0);
-        for (int it = q_issued > C::QST ? q_issued - C::QST : 0; it < q_issued; ++it)
-          mbar_drain(bar(B_FQ + it % C::QST), (it / C::QST) & 1);
-        for (int it = issued > C::OST ? issued - C::OST : 0; it < issued; ++it)
-          mbar_drain(bar(B_FO + it % C::OST), (it / C::OST) & 1);
+      stG[ku % 3] = g - 1;
+      stK[ku % 3] = ku;
+      ++ku;
+    }
+    // let every load this warp started land before shared memory goes away
+    if (lane == 0) {
+      if (kv_issued > 0) {
+        mbar_drain(bar(B_KV), (kv_issued - 1) & 1);
+        mbar_drain(bar(B_V), (kv_issued - 1) & 1);
       }
+      for (int i = q_issued > C::QST ? q_issued - C::QST : 0; i < q_issued; ++i)
+        mbar_drain(bar(B_FQ + i % C::QST), (i / C::QST) & 1);
+      for (int i = o_issued > C::OST ? o_issued - C::OST : 0; i < o_issued; ++i)
+        mbar_drain(bar(B_FO + i % C::OST), (i / C::OST) & 1);
     }
   } else if (warp == 1 || warp == 10) {
     // ------------------------------------------------------------ MMA issuers
     // each issuer warp runs its loop convergently (descriptors stay
     // warp-uniform); lane 0 issues the MMAs and commits
-    if (n_it > 0) {
-      const uint32_t issue = lane == 0 ? 1u : 0u;
-      auto wall = [&](int i, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, err));
+    const uint32_t issue = lane == 0 ? 1u : 0u;
+    auto wall = [&](int i, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, err));
+    };
+    // a K step only moves the descriptor's start address (address >> 4 in
+    // the low 14 bits, all addresses < 232 KB), so a step is one add
+    auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
+    auto kstep = [](int kk) { return (uint32_t)((kk >> 2) * C::ATOM + (kk & 3) * 32); };
+    bool ok = true;
+    int g = 0, ku = 0;
+    if (warp == 1) {
+      // dP^T(g) = V dO_g^T into X(g % 2) once S^T(g) there was read; then
+      // S^T(g+1) = K Q_{g+1}^T into X((g+1) % 2) once Q_{g+1} landed and
+      // dV(g-1), dK(g-1) are done with that buffer.  A unit's first S^T also
+      // waits for the unit's key tile, its first dP^T for the value tile.
+      const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+      const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);   // stage 0
+      const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);  // stage 0
+      auto issue_s = [&](int gg) {
+        const uint64_t q = adv(dQ_km, (gg % C::QST) * C::TILE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tm + (gg & 1) * C::TM_X, adv(dK_km, kstep(kk)), adv(q, kstep(kk)), C::ID_S, kk > 0, issue);
+        mma_commit(bar(B_S + (gg & 1)), issue);
       };
-      // a K step only moves the descriptor's start address (address >> 4 in
-      // the low 14 bits, all addresses < 232 KB), so a step is one add
-      auto adv = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
-      auto kstep = [](int kk) { return (uint32_t)((kk >> 2) * C::ATOM + (kk & 3) * 32); };
-      bool ok = wall(B_KV, 0);
-      if (warp == 1) {
-        // dP^T(i) = V dO_i^T into X(i % 2) once S^T(i) there was read; then
-        // S^T(i+1) = K Q_{i+1}^T into X((i+1) % 2) once Q_{i+1} landed and
-        // dV(i-1), dK(i-1) are done with that buffer
-        const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
-        const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
-        const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);   // stage 0
-        const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);  // stage 0
-        auto issue_s = [&](int it) {
-          const uint64_t q = adv(dQ_km, (it % C::QST) * C::TILE);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tm + (it & 1) * C::TM_X, adv(dK_km, kstep(kk)), adv(q, kstep(kk)), C::ID_S, kk > 0, issue);
-          mma_commit(bar(B_S + (it & 1)), issue);
-        };
-        if ((ok = ok && wall(B_FQ, 0))) {
+      for (int kk = 0; ok && unit_at(kk) < n_units; ++kk) {
+        const int n_it = unit_of(unit_at(kk)).n_it;
+        if (n_it == 0) continue;
+        if (!(ok = wall(B_KV, ku & 1))) break;
+        if (!(ok = wall(B_FQ + g % C::QST, (g / C::QST) & 1))) break;
+        if (g >= 2 && !(ok = wall(B_XF + (g - 2) % C::QST, ((g - 2) / C::QST) & 1))) break;
+        tc_fence_after();
+        issue_s(g);
+        for (int it = 0; it < n_it; ++it, ++g) {
+          if (!(ok = wall(B_SF + (g & 1), (g >> 1) & 1))) break;
+          if (!(ok = wall(B_FO + g % C::OST, (g / C::OST) & 1))) break;
+          if (it == 0 && !(ok = wall(B_V, ku & 1))) break;
           tc_fence_after();
-          issue_s(0);
-        }
-        for (int it = 0; ok && it < n_it; ++it) {
-          if (!(ok = wall(B_SF + (it & 1), (it >> 1) & 1))) break;
-          if (!(ok = wall(B_FO + it % C::OST, (it / C::OST) & 1))) break;
-          tc_fence_after();
-          const uint64_t o = adv(dO_km, (it % C::OST) * C::TILE);
+          const uint64_t o = adv(dO_km, (g % C::OST) * C::TILE);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tm + (it & 1) * C::TM_X, adv(dV_km, kstep(kk)), adv(o, kstep(kk)), C::ID_S, kk > 0, issue);
-          mma_commit(bar(B_DP + (it & 1)), issue);
+          for (int kk2 = 0; kk2 < D / 16; ++kk2)
+            mma_ss(tm + (g & 1) * C::TM_X, adv(dV_km, kstep(kk2)), adv(o, kstep(kk2)), C::ID_S, kk2 > 0, issue);
+          mma_commit(bar(B_DP + (g & 1)), issue);
           if (it + 1 < n_it) {
-            if (!(ok = wall(B_FQ + (it + 1) % C::QST, ((it + 1) / C::QST) & 1))) break;
-            if (it > 0 && !(ok = wall(B_XF + (it - 1) % C::QST, ((it - 1) / C::QST) & 1))) break;
+            if (!(ok = wall(B_FQ + (g + 1) % C::QST, ((g + 1) / C::QST) & 1))) break;
+            if (g >= 1 && !(ok = wall(B_XF + (g - 1) % C::QST, ((g - 1) / C::QST) & 1))) break;
             tc_fence_after();
-            issue_s(it + 1);
+            issue_s(g + 1);
           }
         }
-        mma_commit(bar(B_FIN_S), issue);
-        mbar_drain(bar(B_FIN_S), 0);
-      } else if (warp == 10) {
-        // dV += P^T dO_i and dK += dS^T Q_i once the softmax warps wrote
-        // P^T(i), dS^T(i) into X: packed bf16, queries 32 g .. 32 g + 31 at
-        // columns 32 g + 0..15 (P) and 32 g + 16..31 (dS)
-        const uint64_t dO_mn = sdesc_sw128(sbase + C::OFF_DO, C::ATOM, 1024);  // stage 0, MN-major
-        const uint64_t dQ_mn = sdesc_sw128(sbase + C::OFF_Q, C::ATOM, 1024);
-        auto p_col = [](int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); };
-        for (int it = 0; ok && it < n_it; ++it) {
-          if (!(ok = wall(B_DS + (it & 1), (it >> 1) & 1))) break;
-          tc_fence_after();
-          const uint64_t o = adv(dO_mn, (it % C::OST) * C::TILE), q = adv(dQ_mn, (it % C::QST) * C::TILE);
-          const uint32_t xb = tm + (it & 1) * C::TM_X;
-#pragma unroll
-          for (int kk = 0; kk < C::BQ / 16; ++kk)
-            mma_ts(tm + C::TM_DV, xb + p_col(kk), adv(o, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u, issue);
-#pragma unroll
-          for (int kk = 0; kk < C::BQ / 16; ++kk)
-            mma_ts(tm + C::TM_DK, xb + 16 + p_col(kk), adv(q, kk * 2048), C::ID_DVK, (it > 0 || kk > 0) ? 1u : 0u,
-                   issue);
-          mma_commit(bar(B_XF + it % C::QST), issue);
-        }
-        // every dV/dK MMA (the last depends on every S^T and dP^T MMA) must
-        // finish before the epilogue reads dV, dK and tensor memory is released
-        mma_commit(bar(B_FINAL), issue);
-        mbar_drain(bar(B_FINAL), 0);
+        ++ku;
       }
+      mma_commit(bar(B_FIN_S), issue);
+      mbar_drain(bar(B_FIN_S), 0);
+    } else {
+      // dV += P^T dO_g and dK += dS^T Q_g once the softmax warps wrote
+      // P^T(g), dS^T(g) into X: packed bf16, queries 32 c .. 32 c + 31 at
+      // columns 32 c + 0..15 (P) and 32 c + 16..31 (dS).  A unit's first
+      // products wait for the previous unit's epilogue to have read dV, dK;
+      // after its last, this warp writes the staged dV, dK out.
+      const uint64_t dO_mn = sdesc_sw128(sbase + C::OFF_DO, C::ATOM, 1024);  // stage 0, MN-major
+      const uint64_t dQ_mn = sdesc_sw128(sbase + C::OFF_Q, C::ATOM, 1024);
+      auto p_col = [](int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); };
+      for (int kk = 0; ok && unit_at(kk) < n_units; ++kk) {
+        const Unit x = unit_of(unit_at(kk));
+        if (x.n_it == 0) continue;
+        for (int it = 0; it < x.n_it; ++it, ++g) {
+          if (!(ok = wall(B_DS + (g & 1), (g >> 1) & 1))) break;
+          if (it == 0 && ku > 0 && !(ok = wall(B_DF, (ku - 1) & 1))) break;
+          tc_fence_after();
+          const uint64_t o = adv(dO_mn, (g % C::OST) * C::TILE), q = adv(dQ_mn, (g % C::QST) * C::TILE);
+          const uint32_t xb = tm + (g & 1) * C::TM_X;
+#pragma unroll
+          for (int kk2 = 0; kk2 < C::BQ / 16; ++kk2)
+            mma_ts(tm + C::TM_DV, xb + p_col(kk2), adv(o, kk2 * 2048), C::ID_DVK, (it > 0 || kk2 > 0) ? 1u : 0u,
+                   issue);
+#pragma unroll
+          for (int kk2 = 0; kk2 < C::BQ / 16; ++kk2)
+            mma_ts(tm + C::TM_DK, xb + 16 + p_col(kk2), adv(q, kk2 * 2048), C::ID_DVK, (it > 0 || kk2 > 0) ? 1u : 0u,
+                   issue);
+          mma_commit(bar(B_XF + g % C::QST), issue);
+        }
+        // the unit's dV, dK (the last product depends on every S^T and dP^T
+        // MMA of the unit) are complete for the epilogue
+        mma_commit(bar(B_FINAL), issue);
+        if (!ok) break;
+        // once the softmax warps staged dV, dK: write them out, and release
+        // the staging once the stores have read it
+        if (!(ok = wall(B_STG, ku & 1))) break;
+        if (lane == 0) {
+          // three groups: dV's first half (key tile), its second (value
+          // tile), dK (ring stages), each released once the stores read it
+          const int G = g - 1;
+          const int kvrow = x.b * (int)p.Hkv + x.hkv;
+          for (int a = 0; a < D / 32; ++a) {
+            tma_store_3d(&tmDV, sbase + C::OFF_K + a * C::ATOM, a * 32, x.m0, kvrow);
+            if (a + 1 == D / 64 || a + 1 == D / 32) bulk_commit_group();
+          }
+          for (int a = 0; a < D / 32; ++a) {
+            const uint32_t src = a < D / 64 ? sbase + C::OFF_Q + (uint32_t)(G % C::QST) * C::TILE + a * C::ATOM
+                                            : sbase + C::OFF_DO + (uint32_t)(G % C::OST) * C::TILE +
+                                                  (a - D / 64) * C::ATOM;
+            tma_store_3d(&tmDK, src, a * 32, x.m0, kvrow);
+          }
+          bulk_commit_group();
+          bulk_wait_read_2();
+          counter_bump(k_cnt);
+          bulk_wait_read_1();
+          counter_bump(v_cnt);
+          bulk_wait_read_all();
+          counter_bump(r_cnt);
+        }
+        __syncwarp();
+        ++ku;
+      }
+      if (lane == 0) bulk_wait_read_all();  // (every group was waited for above; kept for an early exit)
+      mma_commit(bar(B_FIN_X), issue);
+      mbar_drain(bar(B_FIN_X), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax / dS
     // warps 2-5 take query columns 0-63 of the tile, warps 6-9 columns 64-127
     const int hf = (warp - 2) >> 2;
     const int r = (warp & 3) * 32 + lane;  // key row within the tile
-    const int64_t m = m0 + r;
-    const bool key_in = m < p.M;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c1 = p.scale * kLog2e;
-    // additive mask: this thread's 64 values (its key row, its 64 query
-    // columns), as f16 pairs, loaded once per query tile (the first head of
-    // the group) and kept for the others.  Entries outside the matrix read as
-    // 0; those rows or keys are masked through LSE = +inf or the key bound
-    // anyway.
-    const bool has_mask = p.mask != nullptr;
-    const uint16_t* mrow = p.mask + (key_in ? m : 0);
-    uint32_t mk[32];
-    auto load_mask = [&](int itx) {
-      const int64_t nbx = (qt0 + itx / rk2) * C::BQ + hf * 64;
-      const uint16_t* src = mrow + p.M * nbx;  // walks down the query rows
-      if (key_in && nbx + 64 <= p.N) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const uint32_t lo = __ldg(src);
-          src += p.M;
-          const uint32_t hi = __ldg(src);
-          src += p.M;
-          mk[c] = lo | (hi << 16);
-        }
-      } else {  // key past M or a ragged last query tile
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const bool in0 = key_in && nbx + 2 * c < p.N, in1 = key_in && nbx + 2 * c + 1 < p.N;
-          const uint32_t lo = in0 ? __ldg(src) : 0u;
-          src += p.M;
-          const uint32_t hi = in1 ? __ldg(src) : 0u;
-          src += p.M;
-          mk[c] = lo | (hi << 16);
-        }
-      }
-    };
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int os = it % C::OST;
-      const int64_t nb = (qt0 + it / rk2) * C::BQ + hf * 64;  // first query of this thread's columns
-      if (has_mask && it % rk2 == 0) load_mask(it);
-      ok = mbar_wait(bar(B_FO + os), (it / C::OST) & 1, abort_flag, err);
-      const uint32_t xb = (uint32_t)(it & 1) * C::TM_X;
-      const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-      ok = ok && mbar_wait(bar(B_S + (it & 1)), ph, abort_flag, err);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      uint32_t ra[32], rb[32];
-      tmem_ld32(tm + lane_off + xb + hf * 64, ra);
-      tmem_ld32(tm + lane_off + xb + hf * 64 + 32, rb);
-      tmem_ld_wait2(ra, rb);
-      // S^T(i) is in registers: the buffer may take dP^T(i)
-      tc_fence_before();
-      mbar_arrive(bar(B_SF + (it & 1)));
-      const float4* lse4 = reinterpret_cast<const float4*>(ld_smem + os * 2 * C::BQ + hf * 64);
-      const float4* di4 = reinterpret_cast<const float4*>(ld_smem + os * 2 * C::BQ + C::BQ + hf * 64);
-      float pv[64];
-#pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) {
-        const float4 l4 = lse4[q4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int jj = q4 * 4 + e;
-          pv[jj] = fmaf(__uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]), c1, -lv[e]);
-        }
-      }
-      if (has_mask) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mk[c]));
-          pv[2 * c] = fmaf(mf.x, kLog2e, pv[2 * c]);
-          pv[2 * c + 1] = fmaf(mf.y, kLog2e, pv[2 * c + 1]);
-        }
-      }
-      // queries before the causal diagonal (top-left: key m > query n) and
-      // keys past M; only diagonal tiles and the last key tile have any
-      if ((p.causal && m0 + C::BM - 1 > nb) || m0 + C::BM > p.M) {
-        int64_t lo = 0;  // first allowed column e (query nb + e)
-        if (p.causal && m - nb > lo) lo = m - nb;
-        if (!key_in) lo = 64;
-        const int li = lo > 64 ? 64 : (int)lo;
-#pragma unroll
-        for (int e = 0; e < 64; ++e)
-          if (e < li) pv[e] = -INFINITY;
-      }
-#pragma unroll
-      for (int e = 0; e < 64; ++e) pv[e] = ex2_approx(pv[e]);
-
-      ok = mbar_wait(bar(B_DP + (it & 1)), ph, abort_flag, err);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        // queries 32 g .. 32 g + 31 of this warp's 64: read dP^T, then write
-        // [P^T | dS^T] (16 + 16 packed columns) over the same 32 columns
-        const uint32_t xcol = tm + lane_off + xb + hf * 64 + g * 32;
-        tmem_ld32(xcol, ra);
-        tmem_ld_wait(ra);
-        uint32_t pk[32];
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 d4 = di4[g * 8 + q4];
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-          for (int e = 0; e < 4; e += 2) {
-            const int jj = q4 * 4 + e;  // column within the half
-            const float p0 = pv[g * 32 + jj], p1 = pv[g * 32 + jj + 1];
-            pk[jj >> 1] = pack_bf16x2(p0, p1);
-            pk[16 + (jj >> 1)] =
-                pack_bf16x2(p0 * (__uint_as_float(ra[jj]) - dv[e]), p1 * (__uint_as_float(ra[jj + 1]) - dv[e + 1]));
+    uint32_t mk[MASK ? 32 : 1];
+    int g = 0, ku = 0;
+    for (int kk = 0; unit_at(kk) < n_units; ++kk) {
+      const Unit x = unit_of(unit_at(kk));
+      const int m = x.m0 + r;  // this thread's key (< 2^31)
+      const bool key_in = m < p.M;
+      if (x.n_it == 0) {
+        // no query reaches these keys: dK = dV = 0
+        if (key_in) {
+          const int64_t row = ((int64_t)x.b * p.Hkv + x.hkv) * p.M + m;
+          float* dst_v = p.dv + row * D + hf * (D / 2);
+          float* dst_k = p.dk + row * D + hf * (D / 2);
+          for (int c = 0; c < D / 2; c += 4) {
+            *reinterpret_cast<float4*>(dst_v + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(dst_k + c) = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
-        tmem_st32(xcol, pk);
+        continue;
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(B_DS + (it & 1)));
-    }
-    // epilogue: dV and dK (scaled) of this key tile, half of the columns per
-    // warp, staged in the now idle tile area (dV from 0, dK from D * 512
-    // bytes) as 32-column atoms of 128-byte swizzled rows, then written by
-    // bulk tensor stores (rows past M are clipped by the store).  The
-    // tensor-memory loads are warp collectives, so every lane runs them.
-    const bool done = n_it > 0 && mbar_wait(bar(B_FINAL), 0, abort_flag, err);
-    const bool write = __all_sync(0xffffffffu, done && !*abort_flag);
-    if (write) {
+      // additive mask: this thread's 64 values (its key row, its 64 query
+      // columns), as f16 pairs, loaded once per query tile (the first head of
+      // the group) and kept for the others.  Entries outside the matrix read
+      // as 0; those rows or keys are masked through LSE = +inf or the key
+      // bound anyway.
+      auto load_mask = [&](int nbx) {  // nbx = the first of the thread's 64 queries
+        if (!MASK) return;
+        const uint16_t* src = p.mask + (key_in ? m : 0) + p.M * nbx;  // walks down the query rows
+        if (key_in && nbx + 64 <= p.N) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t lo = __ldg(src);
+            src += p.M;
+            const uint32_t hi = __ldg(src);
+            src += p.M;
+            mk[c] = lo | (hi << 16);
+          }
+        } else {  // key past M or a ragged last query tile
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const bool in0 = key_in && nbx + 2 * c < p.N, in1 = key_in && nbx + 2 * c + 1 < p.N;
+            const uint32_t lo = in0 ? __ldg(src) : 0u;
+            src += p.M;
+            const uint32_t hi = in1 ? __ldg(src) : 0u;
+            src += p.M;
+            mk[c] = lo | (hi << 16);
+          }
+        }
+      };
+      bool ok = true;
+      // tiles walk query tile by query tile, each for every head of the group
+      int nb = x.qt0 * C::BQ + hf * 64;  // first query of this thread's columns
+      int hc = 0;                        // head within the group
+      for (int left = x.n_it; left > 0; --left, ++g) {
+        const int os = g % C::OST;
+        if (MASK && hc == 0) load_mask(nb);
+        ok = mbar_wait(bar(B_FO + os), (g / C::OST) & 1, abort_flag, err);
+        const uint32_t xb = (uint32_t)(g & 1) * C::TM_X;
+        const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+        ok = ok && mbar_wait(bar(B_S + (g & 1)), ph, abort_flag, err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tm + lane_off + xb + hf * 64, ra);
+        tmem_ld32(tm + lane_off + xb + hf * 64 + 32, rb);
+        tmem_ld_wait2(ra, rb);
+        // S^T(g) is in registers: the buffer may take dP^T(g)
+        tc_fence_before();
+        mbar_arrive(bar(B_SF + (g & 1)));
+        const float4* lse4 = reinterpret_cast<const float4*>(ld_smem + os * 2 * C::BQ + hf * 64);
+        const float4* di4 = reinterpret_cast<const float4*>(ld_smem + os * 2 * C::BQ + C::BQ + hf * 64);
+        float pv[64];
+#pragma unroll
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 l4 = lse4[q4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int jj = q4 * 4 + e;
+            pv[jj] = fmaf(__uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]), c1, -lv[e]);
+          }
+        }
+        if (MASK) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mk[c]));
+            pv[2 * c] = fmaf(mf.x, kLog2e, pv[2 * c]);
+            pv[2 * c + 1] = fmaf(mf.y, kLog2e, pv[2 * c + 1]);
+          }
+        }
+        // queries before the causal diagonal (top-left: key m > query n) and
+        // keys past M; only diagonal tiles and the last key tile have any
+        if ((p.causal && m - r + C::BM - 1 > nb) || m - r + C::BM > p.M) {
+          int lo = 0;  // first allowed column e (query nb + e)
+          if (p.causal && m - nb > lo) lo = m - nb;
+          if (!key_in) lo = 64;
+          const int li = lo > 64 ? 64 : lo;
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e < li) pv[e] = -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < 64; ++e) pv[e] = ex2_approx(pv[e]);
+
+        ok = mbar_wait(bar(B_DP + (g & 1)), ph, abort_flag, err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          // queries 32 hh .. 32 hh + 31 of this warp's 64: read dP^T, then
+          // write [P^T | dS^T] (16 + 16 packed columns) over the same 32 columns
+          const uint32_t xcol = tm + lane_off + xb + hf * 64 + hh * 32;
+          tmem_ld32(xcol, ra);
+          tmem_ld_wait(ra);
+          uint32_t pk[32];
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 d4 = di4[hh * 8 + q4];
+            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+              const int jj = q4 * 4 + e;  // column within the half
+              const float p0 = pv[hh * 32 + jj], p1 = pv[hh * 32 + jj + 1];
+              pk[jj >> 1] = pack_bf16x2(p0, p1);
+              pk[16 + (jj >> 1)] = pack_bf16x2(p0 * (__uint_as_float(ra[jj]) - dv[e]),
+                                               p1 * (__uint_as_float(ra[jj + 1]) - dv[e + 1]));
+            }
+          }
+          tmem_st32(xcol, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(B_DS + (g & 1)));
+        if (++hc == rk2) {
+          hc = 0;
+          nb += C::BQ;
+        }
+      }
+      if (!ok) break;
+      // epilogue: dV and dK (scaled) of this key tile, half of the columns
+      // per warp, as 32-column atoms of 128-byte swizzled rows: dV in the
+      // key/value tiles, dK's first D/2 columns in the Q stage of the unit's
+      // last tile G, the rest in its dO stage (every product reading them is
+      // done; the producer holds the next loads into them until the stores
+      // have read them).  The dV/dK issuer writes them out (rows past M are
+      // clipped by the store).  The tensor-memory loads are warp
+      // collectives, so every lane runs them.
+      const int G = g - 1;
+      const bool done = mbar_wait(bar(B_FINAL), ku & 1, abort_flag, err);
+      const bool write = __all_sync(0xffffffffu, done && !*abort_flag);
+      if (!write) break;
       tc_fence_after();
 #pragma unroll 1
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
@@ -489,8 +665,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tm + lane_off + C::TM_DV + hf * (D / 2) + c0, rv);
         tmem_ld32(tm + lane_off + C::TM_DK + hf * (D / 2) + c0, rk);
         tmem_ld_wait2(rv, rk);
-        const uint32_t rowv = sbase + C::OFF_STAGE + (uint32_t)((hf * (D / 2) + c0) / 32) * C::ATOM + r * 128;
-        const uint32_t rowk = rowv + C::STAGE_DK;
+        const int a = (hf * (D / 2) + c0) / 32;  // atom (32 columns)
+        const uint32_t rowv = sbase + C::OFF_K + (uint32_t)a * C::ATOM + r * 128;
+        const uint32_t rowk = (a < D / 64 ? sbase + C::OFF_Q + (uint32_t)(G % C::QST) * C::TILE + (uint32_t)a * C::ATOM
+                                          : sbase + C::OFF_DO + (uint32_t)(G % C::OST) * C::TILE +
+                                                (uint32_t)(a - D / 64) * C::ATOM) +
+                              r * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k ^ (r & 7)) << 4;
@@ -502,27 +682,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       fence_proxy_async_smem();
-    } else if (n_it == 0 && key_in) {
-      // no query reaches these keys: dK = dV = 0
-      const int64_t row = (b * p.Hkv + hkv) * p.M + m;
-      float* dst_v = p.dv + row * D + hf * (D / 2);
-      float* dst_k = p.dk + row * D + hf * (D / 2);
-      for (int c = 0; c < D / 2; c += 4) {
-        *reinterpret_cast<float4*>(dst_v + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(dst_k + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    named_bar_sync(1, kSoftmaxThreads);
-    if (warp == 2 && lane == 0 && write) {
-      const int kvrow = (int)(b * p.Hkv + hkv);
-      for (int a = 0; a < D / 32; ++a) {
-        tma_store_3d(&tmDV, sbase + C::OFF_STAGE + a * C::ATOM, a * 32, (int)m0, kvrow);
-        tma_store_3d(&tmDK, sbase + C::OFF_STAGE + C::STAGE_DK + a * C::ATOM, a * 32, (int)m0, kvrow);
-      }
-      bulk_commit_group();
-      // the stores must have read shared memory before the CTA exits (their
-      // global writes complete before the grid does)
-      bulk_wait_read_all();
+      // dV, dK have been read: the next unit's first products may overwrite
+      // them; and they are staged: the dV/dK issuer writes them out
+      tc_fence_before();
+      mbar_arrive(bar(B_DF));
+      mbar_arrive(bar(B_STG));
+      ++ku;
     }
   }
 
@@ -545,7 +710,7 @@ bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* di
   return r == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool MASK>
 cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   using C = Cfg<D>;
   CUtensorMap mq, mk, mv, mo, mdk, mdv;
@@ -591,10 +756,16 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   p.mask = pr.mask;
   p.dk = pr.packed + pr.off_k / 4;
   p.dv = pr.packed + pr.off_v / 4;
-  const int64_t grid = ((pr.M + C::BM - 1) / C::BM) * pr.Hkv * pr.B;
-  cudaError_t err = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  // persistent: one CTA per SM (each owns the SM's tensor memory), walking units
+  const int64_t units = ((pr.M + C::BM - 1) / C::BM) * pr.Hkv * pr.B;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  const int64_t grid = units < sms ? units : sms;
+  cudaError_t err =
+      cudaFuncSetAttribute(bwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  bwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdk, mdv, p);
+  bwd_tc_kernel<D, MASK><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdk, mdv, p);
   return cudaPeekAtLastError();
 }
 
@@ -605,12 +776,15 @@ bool backward_tc_supported(const Problem& p) {
   if (p.DK != 64 && p.DK != 128) return false;
   // TMA coordinates are 32-bit; grid.x must fit as well
   if (p.N >= (1ll << 31) || p.M >= (1ll << 31) || p.H * p.B >= (1ll << 31)) return false;
-  if (((p.N + 127) / 128) * p.H * p.B >= (1ll << 31)) return false;  // query-pass grid
+  if (((p.N + 127) / 128) * p.H * p.B >= (1ll << 31)) return false;  // query-pass units
+  if (((p.M + 127) / 128) * p.Hkv * p.B >= (1ll << 31)) return false;  // key-pass units
   return true;
 }
 
 cudaError_t launch_backward_tc(const Problem& p, cudaStream_t s) {
-  return p.DK == 128 ? launch_d<128>(p, s) : launch_d<64>(p, s);
+  const bool m = p.mask != nullptr;
+  if (p.DK == 128) return m ? launch_d<128, true>(p, s) : launch_d<128, false>(p, s);
+  return m ? launch_d<64, true>(p, s) : launch_d<64, false>(p, s);
 }
 
 uint32_t take_error_tc() {

@@ -154,6 +154,18 @@ FAB_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 
 // As bulk_wait_read_all, but only for all but the most recent group.
 FAB_DEV void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
+// As bulk_wait_read_all, but only for all but the two most recent groups.
+FAB_DEV void bulk_wait_read_2() { asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); }
+
+// Tiled bulk prefetch global -> L2 (no destination, no completion): warms L2
+// for a later tma_load_3d of the same box.
+FAB_DEV void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // Waits until every bulk store this thread committed has completed (global
 // writes done, shared memory free).
 FAB_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

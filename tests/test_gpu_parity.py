@@ -37,6 +37,10 @@ SMALL = [
     ("tc64_causal", 2, 2, 2, 256, 256, 64, 64, "bf16", True, "none"),
     ("tc64_mask_gqa_ragged", 1, 4, 2, 70, 130, 64, 64, "bf16", False, "random"),
     ("tc128_single", 1, 1, 1, 1, 1, 128, 128, "bf16", False, "none"),
+    # more work units than SMs, so each persistent CTA walks several; causal
+    # units of 1..5 tiles put short units back to back
+    ("tc64_causal_many_units", 8, 8, 8, 640, 640, 64, 64, "bf16", True, "none"),
+    ("tc128_gqa_mask_many_units", 16, 8, 4, 384, 384, 128, 128, "bf16", True, "random"),
     ("simt_f32_odd", 1, 2, 1, 40, 50, 16, 24, "f32", True, "none"),
     ("simt_f32_mask", 2, 2, 2, 33, 65, 64, 64, "f32", False, "random"),
     ("simt_bf16_odd", 1, 2, 1, 33, 47, 40, 24, "bf16", False, "random"),
