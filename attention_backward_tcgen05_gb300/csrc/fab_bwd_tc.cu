@@ -9,12 +9,13 @@
 // log-sum-exp), dV = P^T dO, dP = dO V^T, dS = P * (dP - D), dK = scale dS^T Q.
 // D_i = dO_i . O_i comes from the preprocess kernel.
 //
-// Decomposition: one CTA per (key tile of BM = 128 keys, key/value head,
-// batch).  The key/value tile stays in shared memory; the CTA walks every
-// query tile of BQ = 128 queries (skipping tiles a top-left causal mask
-// empties) and, for each, every query head of the GQA group, so dK and dV of
-// the group accumulate in tensor memory without atomics and the additive
-// mask tile (shared by all heads) is read once per query tile.
+// Decomposition: work units of (key tile of BM = 128 keys, key/value head,
+// batch); persistent CTAs, one per SM, walk them.  A unit's key/value tile
+// stays in shared memory; the unit walks every query tile of BQ = 128
+// queries (skipping tiles a top-left causal mask empties) and, for each,
+// every query head of the GQA group, so dK and dV of the group accumulate in
+// tensor memory without atomics and the additive mask tile (shared by all
+// heads) is read once per query tile.
 //
 // Per query tile, in the transposed ("key rows") orientation so that one
 // thread owns one key row of every tensor-memory tile:
@@ -52,10 +53,10 @@
 // streams those stalls overlap the other stream's MMAs.
 //
 // Warps (352 threads): 0 = TMA producer (and the tile's LSE and D rows);
-// 1 = tensor-memory allocator and S^T/dP^T issuer; 10 = dV/dK issuer (lane 0
-// of an issuer warp issues); 2-9 = softmax/dS and the epilogue (thread = key
-// row; two warps per tensor-memory lane quarter, each taking 64 of the
-// tile's 128 queries).  All hand-offs are mbarriers; every wait is bounded
+// 1 = tensor-memory allocator and S^T/dP^T issuer; 10 = dV/dK issuer and the
+// epilogue's bulk stores (lane 0 of an issuer warp issues); 2-9 = softmax/dS
+// and the epilogue staging (thread = key row; two warps per tensor-memory
+// lane quarter, each taking 64 of the tile's 128 queries).  All hand-offs are mbarriers; every wait is bounded
 // (see fab_device.cuh).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
