@@ -26,7 +26,8 @@ FAB_OK, FAB_ERR_INVALID, FAB_ERR_UNSUPPORTED, FAB_ERR_WORKSPACE, FAB_ERR_CUDA, F
 FAB_F32, FAB_BF16 = 0, 1
 
 EXPORTS = ("fab_version", "fab_status_string", "fab_packed_offsets", "fab_packed_bytes",
-           "fab_backward_workspace_bytes", "fab_forward_lse", "fab_backward", "fab_backward_preprocess",
+           "fab_backward_workspace_bytes", "fab_backward_recompute_workspace_bytes", "fab_forward_lse",
+           "fab_backward", "fab_backward_preprocess",
            "fab_backward_main", "fab_backward_query_pass", "fab_backward_key_pass", "fab_backward_noalloc",
            "fab_last_device_error")
 NOALLOC_MAX_ROWS = 1048576  # FAB_NOALLOC_MAX_ROWS
@@ -67,6 +68,7 @@ def lib():
                     "fab_packed_offsets": ([dp, szp, szp, szp], i32),
                     "fab_packed_bytes": ([dp], sz),
                     "fab_backward_workspace_bytes": ([dp, i32], sz),
+                    "fab_backward_recompute_workspace_bytes": ([dp, i32], sz),
                     "fab_forward_lse": ([vp, vp, vp, vp, i32, f32, i32, dp, vp, vp, vp], i32),
                     "fab_backward": ([vp, vp, vp, vp, vp, vp, vp, i32, f32, i32, dp, vp, sz, vp, vp], i32),
                     "fab_backward_preprocess": ([vp, vp, i32, dp, vp, sz, vp, vp], i32),
@@ -162,6 +164,10 @@ def fab_backward_workspace_bytes(dims: fab_dims, dtype: int) -> int:
     return lib().fab_backward_workspace_bytes(ctypes.byref(dims), int(dtype))
 
 
+def fab_backward_recompute_workspace_bytes(dims: fab_dims, dtype: int) -> int:
+    return lib().fab_backward_recompute_workspace_bytes(ctypes.byref(dims), int(dtype))
+
+
 def fab_forward_lse(q, k, v, mask, causal, scale, o, lse, stream=None):
     dims = dims_of(q, k, v)
     t = dtype_code(q)
@@ -173,11 +179,14 @@ def fab_forward_lse(q, k, v, mask, causal, scale, o, lse, stream=None):
 
 
 def fab_backward(q, k, v, d, o, lse, mask, causal, scale, workspace, packed_out, stream=None):
+    """o and lse may both be None: the library then recomputes them into the
+    workspace (sized by fab_backward_recompute_workspace_bytes)."""
     dims = dims_of(q, k, v)
     t = dtype_code(q)
     oshape = (dims.B, dims.N, dims.H, dims.DV)
     args = (_dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), _dev(d, "d", q.dtype, oshape),
-            _dev(o, "o", q.dtype, oshape), _dev(lse, "lse", torch.float32, (dims.B, dims.H, dims.N)),
+            None if o is None else _dev(o, "o", q.dtype, oshape),
+            None if lse is None else _dev(lse, "lse", torch.float32, (dims.B, dims.H, dims.N)),
             _mask(mask, dims), int(bool(causal)), float(scale), t, ctypes.byref(dims),
             _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
             _dev(packed_out, "packed_out", torch.float32, (fab_packed_bytes(dims) // 4,)), _stream(stream))
@@ -262,18 +271,20 @@ def forward(q, k, v, mask=None, causal=False, scale=None, stream=None):
     return o, lse
 
 
-def alloc_backward(dims: fab_dims, dtype: int, device):
-    """(workspace uint8 tensor, packed float32 tensor) sized for fab_backward."""
-    ws = torch.empty(max(fab_backward_workspace_bytes(dims, dtype), 16), dtype=torch.uint8, device=device)
+def alloc_backward(dims: fab_dims, dtype: int, device, recompute: bool = False):
+    """(workspace uint8 tensor, packed float32 tensor) sized for fab_backward
+    (recompute: for a call without o and lse)."""
+    wsb = fab_backward_recompute_workspace_bytes(dims, dtype) if recompute else fab_backward_workspace_bytes(dims, dtype)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
     packed = torch.empty(fab_packed_bytes(dims) // 4, dtype=torch.float32, device=device)
     return ws, packed
 
 
-def backward(q, k, v, d, o, lse, mask=None, causal=False, scale=None, stream=None):
-    """Returns the packed f32 [dQ | dK | dV] buffer."""
+def backward(q, k, v, d, o=None, lse=None, mask=None, causal=False, scale=None, stream=None):
+    """Returns the packed f32 [dQ | dK | dV] buffer (o, lse None: recomputed)."""
     dims = dims_of(q, k, v)
     scale = dims.DK ** -0.5 if scale is None else scale
-    ws, packed = alloc_backward(dims, dtype_code(q), q.device)
+    ws, packed = alloc_backward(dims, dtype_code(q), q.device, recompute=o is None and lse is None)
     fab_backward(q, k, v, d, o, lse, mask, causal, scale, ws, packed, stream)
     return packed
 

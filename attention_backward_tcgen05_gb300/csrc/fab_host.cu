@@ -67,6 +67,14 @@ size_t di_bytes(const fab_dims* d) {
   return (b + 255) / 256 * 256;
 }
 
+// The forward output O [DV,H,N,B] and the row LSE [N,H,B] that fab_backward
+// keeps in its workspace, after D_i, when the caller passes neither.
+size_t o_bytes(const fab_dims* d, int dtype) {
+  const size_t b = (size_t)(d->B * d->H * d->N * d->DV) * (dtype == FAB_BF16 ? 2u : 4u);
+  return (b + 255) / 256 * 256;
+}
+size_t recompute_bytes(const fab_dims* d, int dtype) { return di_bytes(d) + o_bytes(d, dtype) + di_bytes(d); }
+
 Problem make_problem(const fab_dims* d, int dtype, float scale, int causal) {
   Problem p{};
   p.B = d->B;
@@ -151,6 +159,11 @@ FAB_API size_t fab_packed_bytes(const fab_dims* dims) {
 FAB_API size_t fab_backward_workspace_bytes(const fab_dims* dims, int dtype) {
   if (check_dims(dims) != FAB_OK || !dtype_ok(dtype)) return 0;
   return di_bytes(dims);
+}
+
+FAB_API size_t fab_backward_recompute_workspace_bytes(const fab_dims* dims, int dtype) {
+  if (check_dims(dims) != FAB_OK || !dtype_ok(dtype)) return 0;
+  return recompute_bytes(dims, dtype);
 }
 
 FAB_API int fab_forward_lse(const void* q, const void* k, const void* v, const uint16_t* mask, int causal,
@@ -271,6 +284,23 @@ FAB_API int fab_backward_key_pass(const void* q, const void* k, const void* v, c
 FAB_API int fab_backward(const void* q, const void* k, const void* v, const void* d, const void* o, const float* lse,
                          const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims,
                          void* workspace, size_t workspace_bytes, float* packed_out, fab_stream stream) {
+  if (o == nullptr || lse == nullptr) {
+    // ggml_flash_attn_back's operands are q, k, v, the mask and d alone: with
+    // neither o nor lse given, the forward is recomputed into the workspace
+    // (after D_i) before the backward proper
+    if (o != nullptr || lse != nullptr) return FAB_ERR_INVALID;
+    const void* ptrs4[4] = {q, k, v, d};
+    int rc0 = check_backward(dims, dtype, ptrs4, 4, mask, workspace, workspace_bytes, packed_out);
+    if (rc0 != FAB_OK) return rc0;
+    if (workspace_bytes < recompute_bytes(dims, dtype)) return FAB_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* o2 = ws + di_bytes(dims);
+    float* lse2 = reinterpret_cast<float*>(ws + di_bytes(dims) + o_bytes(dims, dtype));
+    rc0 = fab_forward_lse(q, k, v, mask, causal, scale, dtype, dims, o2, lse2, stream);
+    if (rc0 != FAB_OK) return rc0;
+    o = o2;
+    lse = lse2;
+  }
   const void* ptrs[6] = {q, k, v, d, o, lse};
   int rc = check_backward(dims, dtype, ptrs, 6, mask, workspace, workspace_bytes, packed_out);
   if (rc != FAB_OK) return rc;

@@ -53,6 +53,7 @@ extern "C" FAB_EXPORT int fab_backward_noalloc(const void* q, const void* k, con
                                                float scale, int dtype, const fab_dims* dims, float* packed_out,
                                                fab_stream stream) {
   if (dims == nullptr || dims->B <= 0 || dims->H <= 0 || dims->N <= 0) return FAB_ERR_INVALID;
+  if (o == nullptr || lse == nullptr) return FAB_ERR_INVALID;  // the fixed scratch holds D_i only
   // B*H*N rows of D_i must fit the fixed array (checked without overflow)
   if (dims->B > fab::kMaxRows || dims->H > fab::kMaxRows / dims->B || dims->N > fab::kMaxRows / (dims->B * dims->H))
     return FAB_ERR_WORKSPACE;

@@ -10,7 +10,8 @@ fab_backward_preprocess then fab_backward_main.  Throughput counts
 the dominant kernel's roofline against the measured dense bf16 peak, an
 end-to-end number with host buffers (pinned H2D copies of the inputs,
 fab_backward, D2H of the packed gradients), the forward kernel's TFLOP/s,
-and the fp64 CPU oracle timed on a bounded sample.
+fab_backward without o and lse (the forward recomputed inside), and the
+fp64 CPU oracle timed on a bounded sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl fab|reference]
 
@@ -245,6 +246,23 @@ def run_fab(args, rank, world, local):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     tensor_core = w.dtype == "bf16" and w.DK == w.DV and w.DK in (64, 128)
 
+    # fab_backward without o and lse (the op's own operands only): the forward
+    # is recomputed into the workspace first; timed on its own, L2 flushed
+    rec_ms = []
+    if args.forward_steps:
+        ws_r, packed_r = binding.alloc_backward(dims, dt, dev, recompute=True)
+        flush_r = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        for i in range(4):
+            flush_r.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            binding.fab_backward(q, k, v, d, None, None, mask, w.causal, w.scale, ws_r, packed_r)
+            e1.record(stream)
+            e1.synchronize()
+            if i > 0:
+                rec_ms.append(e0.elapsed_time(e1))
+        del ws_r, packed_r, flush_r
+
     # the two launches of one backward step (what fab_backward enqueues)
     if tensor_core:
         stage_names = ("query_pass", "key_pass")
@@ -425,6 +443,11 @@ def run_fab(args, rank, world, local):
                          "ms": round(statistics.median(fwd_ms), 3),
                          "kernel": "fwd_tc_kernel" if tensor_core else "fwd_simt_kernel"}
                         if fwd_ms else None),
+            "recompute": ({"ms": round(statistics.median(rec_ms), 3),
+                           "tflops_fwd_plus_bwd": round((forward_flops(w) + flops) / (statistics.median(rec_ms) / 1e3)
+                                                        / 1e12, 2),
+                           "note": "fab_backward with o and lse NULL: forward recomputed, then the backward"}
+                          if rec_ms else None),
         }
         print(json.dumps(line), flush=True)
 

@@ -106,6 +106,11 @@ FAB_EXPORT size_t fab_packed_bytes(const fab_dims* dims);
  * f32 [N,H,B]).  0 for bad dims. */
 FAB_EXPORT size_t fab_backward_workspace_bytes(const fab_dims* dims, int dtype);
 
+/* Device workspace bytes fab_backward needs when called without o and lse
+ * (it then recomputes them): D_i, then O (`dtype`, [DV,H,N,B]) and LSE (f32,
+ * [N,H,B]), each part a multiple of 256 bytes.  0 for bad dims. */
+FAB_EXPORT size_t fab_backward_recompute_workspace_bytes(const fab_dims* dims, int dtype);
+
 /* Forward pass saving what the backward needs (labml "Flash Attention",
  * "Forward pass" and "Flash Attention Optimization"; ggmlR attn_ref):
  *   o[:, h, n, b] = sum_m softmax_m(scale * q_n . k_m + mask[m + M*n]) v_m
@@ -122,9 +127,12 @@ FAB_EXPORT int fab_forward_lse(const void* q, const void* k, const void* v, cons
  *   dK_m = scale sum_n dS_nm Q_n,
  * with P recomputed from q, k, mask, causal, scale and the saved lse; dK and
  * dV are summed over each GQA group's query heads.  o and lse must come from
- * fab_forward_lse on the same inputs.  d: device, `dtype`, [DV,H,N,B].
- * workspace: device, >= fab_backward_workspace_bytes() bytes, contents
- * overwritten.  packed_out: device f32, fab_packed_bytes() bytes, fully
+ * fab_forward_lse on the same inputs; or both be NULL, as in
+ * ggml_flash_attn_back, whose operands are q, k, v, the mask and d alone:
+ * the call then enqueues fab_forward_lse into the workspace first (exactly one
+ * of them NULL is FAB_ERR_INVALID).  d: device, `dtype`, [DV,H,N,B].
+ * workspace: device, >= fab_backward_workspace_bytes() bytes (with o and lse
+ * NULL: fab_backward_recompute_workspace_bytes()), contents overwritten.  packed_out: device f32, fab_packed_bytes() bytes, fully
  * overwritten (padding written as 0).  Where the tensor-core kernels apply
  * (bf16, DK == DV in {64, 128}) it enqueues fab_backward_query_pass then
  * fab_backward_key_pass; otherwise fab_backward_preprocess then
@@ -167,7 +175,8 @@ FAB_EXPORT int fab_backward_key_pass(const void* q, const void* k, const void* v
  * times batches): its fixed scratch holds one float per such row. */
 #define FAB_NOALLOC_MAX_ROWS 1048576
 
-/* fab_backward for callers that cannot allocate device memory, for example
+/* fab_backward for callers that cannot allocate device memory (o and lse
+ * must be given: the fixed scratch holds D_i only), for example
  * code whose device memory belongs to another allocator, or code that must not
  * call cudaMalloc (which can synchronise the device) on its path.  The pages
  * have no counterpart; the operation and every argument are those of

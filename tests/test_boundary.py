@@ -76,6 +76,19 @@ def test_workspace_bytes(L):
     assert binding.fab_backward_workspace_bytes(d, 7) == 0
 
 
+def test_recompute_workspace_bytes(L):
+    # without o and lse: D_i, O (dtype) and LSE (f32), each rounded up to 256 bytes
+    d = binding.make_dims(2, 4, 2, 100, 70, 64, 48)
+    r256 = lambda x: (x + 255) // 256 * 256
+    rows = 2 * 4 * 100
+    for dt, elem in ((binding.FAB_BF16, 2), (binding.FAB_F32, 4)):
+        want = r256(rows * 4) + r256(rows * 48 * elem) + r256(rows * 4)
+        assert binding.fab_backward_recompute_workspace_bytes(d, dt) == want
+        assert binding.fab_backward_recompute_workspace_bytes(d, dt) > binding.fab_backward_workspace_bytes(d, dt)
+    assert binding.fab_backward_recompute_workspace_bytes(binding.make_dims(1, 3, 2, 1, 1, 1, 1), 1) == 0
+    assert binding.fab_backward_recompute_workspace_bytes(d, 7) == 0
+
+
 FAKE = 0x10000  # 16-byte-aligned non-null pointer; validation fails before it is used
 
 
@@ -109,6 +122,24 @@ def test_workspace_errors(L):
     assert call_backward(L, d, {"ws": None}) == binding.FAB_ERR_WORKSPACE
     assert call_backward(L, d, ws_bytes=16) == binding.FAB_ERR_WORKSPACE
     assert call_backward(L, d, {"ws": FAKE + 8}) == binding.FAB_ERR_WORKSPACE
+
+
+def test_recompute_validation(L):
+    # o and lse both NULL asks for the forward to be recomputed: the workspace
+    # must then hold O and LSE as well; the other checks still apply first
+    d = binding.make_dims(1, 2, 1, 64, 64, 64, 64)
+    small = binding.fab_backward_workspace_bytes(d, binding.FAB_BF16)
+    big = binding.fab_backward_recompute_workspace_bytes(d, binding.FAB_BF16)
+    none = {"o": None, "lse": None}
+    assert call_backward(L, d, none, ws_bytes=small) == binding.FAB_ERR_WORKSPACE
+    assert call_backward(L, d, none, ws_bytes=big - 1) == binding.FAB_ERR_WORKSPACE
+    assert call_backward(L, d, dict(none, q=None), ws_bytes=big) == binding.FAB_ERR_INVALID
+    assert call_backward(L, d, dict(none, d=FAKE + 4), ws_bytes=big) == binding.FAB_ERR_INVALID
+    assert call_backward(L, d, dict(none, packed=None), ws_bytes=big) == binding.FAB_ERR_INVALID
+    assert call_backward(L, binding.make_dims(1, 3, 2, 4, 4, 8, 8), none, ws_bytes=big) == binding.FAB_ERR_INVALID
+    vp = ctypes.c_void_p
+    args = [vp(FAKE)] * 4 + [None, None, None, 0, 1.0, 1, ctypes.byref(d), vp(FAKE), None]
+    assert L.fab_backward_noalloc(*args) == binding.FAB_ERR_INVALID  # its scratch holds D_i only
 
 
 def test_unsupported_width(L):

@@ -197,6 +197,39 @@ def test_every_slice_written_over_garbage(D, causal, mask):
         assert rel_err(got, ref[key]) <= TOL["bf16"], key
 
 
+@pytest.mark.parametrize("case", [("tc128_gqa_causal", 2, 4, 2, 200, 300, 128, 128, "bf16", True, "random"),
+                                  ("simt_f32", 1, 2, 1, 40, 50, 16, 24, "f32", True, "none")], ids=lambda c: c[0])
+def test_backward_without_o_and_lse(case):
+    # o and lse NULL: the library recomputes the forward into the workspace;
+    # the result is the explicit forward-then-backward result, bit for bit,
+    # and meets the oracle at the usual tolerance
+    name, B, H, Hkv, N, M, DK, DV, dtype, causal, mask = case
+    w = inputs.custom(B, H, Hkv, N, M, DK, DV, dtype=dtype, causal=causal, mask=mask, seed=71,
+                      dist="uniform" if dtype == "f32" else "normal", name=name)
+    x = inputs.make(w)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o, lse = binding.forward(g["q"], g["k"], g["v"], g["mask"], w.causal, w.scale)
+    explicit = binding.backward(g["q"], g["k"], g["v"], g["d"], o, lse, g["mask"], w.causal, w.scale)
+    recomputed = binding.backward(g["q"], g["k"], g["v"], g["d"], None, None, g["mask"], w.causal, w.scale)
+    torch.cuda.synchronize()
+    assert binding.fab_last_device_error() == binding.FAB_OK
+    assert torch.equal(explicit, recomputed)
+    dims = binding.dims_of(g["q"], g["k"], g["v"])
+    ws = torch.full((binding.fab_backward_recompute_workspace_bytes(dims, binding.dtype_code(g["q"])),), 255,
+                    dtype=torch.uint8, device="cuda")
+    packed = torch.full((binding.fab_packed_bytes(dims) // 4,), float("nan"), device="cuda")
+    binding.fab_backward(g["q"], g["k"], g["v"], g["d"], None, None, g["mask"], w.causal, w.scale, ws, packed)
+    torch.cuda.synchronize()
+    assert torch.equal(packed, explicit)
+    ref = oracle_ref(w, x)
+    f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
+    dq, dk, dv = binding.unpack(recomputed, dims)
+    gpu = dict(dq=f64(dq), dk=f64(dk), dv=f64(dv), o=f64(o), lse=f64(lse))
+    errs = compare(w, gpu, ref)
+    for key in ("dq", "dk", "dv", "o"):
+        assert errs[key] <= TOL[dtype], (key, errs)
+
+
 @pytest.mark.parametrize("D,causal,mask", [(128, True, "none"), (64, False, "random"), (128, False, "random")])
 def test_two_phase_api_matches_fab_backward(D, causal, mask):
     # fab_backward_preprocess + fab_backward_main (D_i from the preprocess),
