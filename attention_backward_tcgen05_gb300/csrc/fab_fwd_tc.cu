@@ -8,17 +8,21 @@
 // max m, sum l, unnormalised O, per key block); ggmlR attn_ref for the
 // additive mask (added after scaling) and for rows with no finite score.
 //
-// One CTA per (query tile of 128 rows, query head, batch).  Q stays in shared
-// memory; key/value tiles of 128 keys stream through a two-stage TMA ring.
-// S = Q K_j^T lands in one of two tensor-memory buffers, so the MMA for tile
-// j+1 runs while the softmax warps turn tile j into P (bf16, written back over
-// S) and the tensor core then accumulates O += P V_j in tensor memory.  The
-// running max is only raised when a tile's max exceeds it by more than 8 (in
-// log2 units); P is then bounded by 2^8 and O is rescaled in tensor memory
-// only on those rare updates.  Using a stale max is exact: O and l share it.
+// One CTA per (query tile of 128 rows, query head, batch), heavy causal
+// tiles first.  Q stays in shared memory; key/value tiles of 128 keys stream
+// through a three-stage TMA ring.  S = Q K_j^T lands in one of three
+// tensor-memory buffers, so the MMAs for the next tiles run while the softmax
+// warps turn tile j into P (bf16, written back over S) and the tensor core
+// then accumulates O += P V_j in tensor memory.  The running max is only
+// raised when a tile's max exceeds it by more than 8 (in log2 units); P is
+// then bounded by 2^8 and O is rescaled in tensor memory only on those rare
+// updates.  Using a stale max is exact: O and l share it.
 //
-// Warps: 0 = TMA producer, 1 = tensor-memory allocator and MMA issuer,
-// 2-5 = softmax, rescale and epilogue (thread = query row).
+// Warps (352 threads): 0 = TMA producer; 1 = tensor-memory allocator and S
+// issuer; 10 = PV issuer (lane 0 of an issuer warp issues); 2-9 = softmax,
+// rescale and epilogue (thread = query row; two warps per tensor-memory lane
+// quarter, each taking 64 of a tile's 128 keys).  Causal and key-bound tests
+// run only on the tiles that have such keys.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -34,39 +38,45 @@ __device__ uint32_t g_err_fwd;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
-constexpr int kThreads = 192;
+constexpr int kThreads = 352;
+constexpr int kSoftmaxThreads = 256;
 
 template <int D>
 struct FCfg {
   static constexpr int BQ = 128;  // queries per CTA (tensor-memory lanes)
   static constexpr int BK = 128;  // keys per tile
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = 3;
   static constexpr int ATOMS = D / 64;
   static constexpr uint32_t ATOM = 128 * 128;  // one 128-row x 128-byte swizzle atom column
+  static constexpr uint32_t TILE = ATOMS * ATOM;
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + ATOMS * ATOM;
-  static constexpr uint32_t OFF_V = OFF_K + STAGES * ATOMS * ATOM;
-  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * ATOMS * ATOM;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 16 * 8;
-  // at least 116 KB so one CTA owns an SM and its whole tensor memory
-  static constexpr uint32_t SMEM_USED = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t OFF_KV = OFF_Q + TILE;  // stage s: K at + 2 s TILE, V at + (2 s + 1) TILE
+  static constexpr uint32_t OFF_BAR = OFF_KV + STAGES * 2 * TILE;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
+  static constexpr uint32_t OFF_MX = OFF_MISC + 64;  // [2 slots][2 halves][BQ] floats
+  // the swizzled tiles need a 1024-byte-aligned base, checked at run time
+  // (no room for alignment slack at D = 128); at least 116 KB so one CTA
+  // owns an SM and its whole tensor memory
+  static constexpr uint32_t SMEM_USED = OFF_MX + 2 * 2 * BQ * 4;
   static constexpr uint32_t SMEM = SMEM_USED > 118784 ? SMEM_USED : 118784;
-  static constexpr uint32_t TM_S = 0;  // + 128 * buffer
-  static constexpr uint32_t TM_O = 256;
+  static constexpr uint32_t TM_S = 0;  // + 128 * buffer, buffers 0..2
+  static constexpr uint32_t TM_O = 384;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr uint32_t ID_S = idesc_bf16(128, BK, false, false);
   static constexpr uint32_t ID_PV = idesc_bf16(128, D, false, true);
   static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
 };
 
 enum : int {
   F_Q = 0,
-  F_FULL = 1,    // + stage
-  F_EMPTY = 3,   // + stage
-  F_S = 5,       // + buffer
-  F_P = 7,       // + buffer
-  F_PV = 9,      // + buffer
-  F_FINAL = 11,
+  F_FULL = 1,    // + j % 3: K_j and V_j landed
+  F_S = 4,       // + j % 3: S(j) landed
+  F_P = 7,       // + j % 3: softmax warps wrote P(j) (and rescaled O if they had to)
+  F_PV = 10,     // + j % 3: PV(j) finished (its stage, S buffer free; O holds tiles <= j)
+  F_FIN_S = 13,  // every S MMA finished
+  F_FIN_O = 14,  // every PV MMA finished
+  F_COUNT = 15
 };
 
 struct FParams {
@@ -78,27 +88,34 @@ struct FParams {
   float* lse;
 };
 
-template <int D>
+template <int D, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FParams p) {
   using C = FCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem_raw) & 1023u) {  // swizzled tiles need a 1024-byte-aligned base
+    if (threadIdx.x == 0) atomicOr(&g_err_fwd, kErrSmemAlign);
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
+  float* mx = reinterpret_cast<float*>(smem + C::OFF_MX);
   uint32_t* err = &g_err_fwd;
 
   const int warp = (int)warp_id();
   const int lane = (int)lane_id();
 
+  // (query tile, head, batch); heavy (late) query tiles first under a causal mask
   const int64_t q_tiles = (p.N + C::BQ - 1) / C::BQ;
-  const int64_t qt = blockIdx.x % q_tiles;
-  const int64_t bh = blockIdx.x / q_tiles;
-  const int64_t h = bh % p.H, b = bh / p.H;
+  const int64_t hb = p.H * p.B;
+  const int64_t qi = blockIdx.x / hb, rem = blockIdx.x % hb;
+  const int64_t b = rem / p.H, h = rem % p.H;
+  const int64_t qt = p.causal ? q_tiles - 1 - qi : qi;
   const int64_t hkv = h / (p.H / p.Hkv);
   const int64_t n0 = qt * C::BQ;
   int64_t n_kv = (p.M + C::BK - 1) / C::BK;
@@ -111,14 +128,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     mbar_init(bar(F_Q), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(bar(F_FULL + s), 1);
-      mbar_init(bar(F_EMPTY + s), 1);
       mbar_init(bar(F_S + s), 1);
-      mbar_init(bar(F_P + s), 128);
+      mbar_init(bar(F_P + s), kSoftmaxThreads);
       mbar_init(bar(F_PV + s), 1);
     }
-    mbar_init(bar(F_FINAL), 1);
+    mbar_init(bar(F_FIN_S), 1);
+    mbar_init(bar(F_FIN_O), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -132,47 +149,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Q once; K_j, V_j into stage j % 3 once PV(j-3) is done with it
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
-      mbar_arrive_expect_tx(bar(F_Q), C::ATOMS * C::ATOM);
+      mbar_arrive_expect_tx(bar(F_Q), C::TILE);
       for (int a = 0; a < C::ATOMS; ++a)
         tma_load_3d(sbase + C::OFF_Q + a * C::ATOM, &tmQ, bar(F_Q), a * 64, (int)n0, (int)(b * p.H + h));
       int issued = 0;
       const int kvrow = (int)(b * p.Hkv + hkv);
       for (int j = 0; j < nkv; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(bar(F_EMPTY + s), ((j >> 1) & 1) ^ 1, abort_flag, err)) break;
-        mbar_arrive_expect_tx(bar(F_FULL + s), 2 * C::ATOMS * C::ATOM);
+        const int s = j % 3;
+        if (j >= 3 && !mbar_wait(bar(F_PV + s), ((j / 3) - 1) & 1, abort_flag, err)) break;
+        mbar_arrive_expect_tx(bar(F_FULL + s), 2 * C::TILE);
+        const uint32_t sk = sbase + C::OFF_KV + 2 * s * C::TILE;
         for (int a = 0; a < C::ATOMS; ++a) {
-          tma_load_3d(sbase + C::OFF_K + (s * C::ATOMS + a) * C::ATOM, &tmK, bar(F_FULL + s), a * 64,
-                      j * C::BK, kvrow);
-          tma_load_3d(sbase + C::OFF_V + (s * C::ATOMS + a) * C::ATOM, &tmV, bar(F_FULL + s), a * 64,
-                      j * C::BK, kvrow);
+          tma_load_3d(sk + a * C::ATOM, &tmK, bar(F_FULL + s), a * 64, j * C::BK, kvrow);
+          tma_load_3d(sk + C::TILE + a * C::ATOM, &tmV, bar(F_FULL + s), a * 64, j * C::BK, kvrow);
         }
         ++issued;
       }
       mbar_drain(bar(F_Q), 0);
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j) mbar_drain(bar(F_FULL + (j & 1)), (j >> 1) & 1);
+      for (int j = issued > 3 ? issued - 3 : 0; j < issued; ++j) mbar_drain(bar(F_FULL + j % 3), (j / 3) & 1);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // the whole warp runs this loop (descriptors stay warp-uniform); lane 0
-    // issues the MMAs and commits
-    {
-      const uint32_t issue = lane == 0 ? 1u : 0u;
-      auto wall = [&](int i, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, err));
-      };
+  } else if (warp == 1 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // each issuer warp runs its loop convergently (descriptors stay
+    // warp-uniform); lane 0 issues the MMAs and commits
+    const uint32_t issue = lane == 0 ? 1u : 0u;
+    auto wall = [&](int i, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, err));
+    };
+    bool ok = true;
+    if (warp == 1) {
+      // S(j) = Q K_j^T into buffer j % 3 once K_j landed and PV(j-3) is done
+      // with the buffer's P
       const uint32_t sQ = sbase + C::OFF_Q;
-      auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!wall(F_FULL + s, (j >> 1) & 1)) return false;
-        // P(j-2) in this tensor-memory buffer must have been consumed
-        if (j >= 2 && !wall(F_PV + s, ((j >> 1) - 1) & 1)) return false;
+      ok = wall(F_Q, 0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int s = j % 3;
+        if (!(ok = wall(F_FULL + s, (j / 3) & 1))) break;
+        if (j >= 3 && !(ok = wall(F_PV + s, ((j / 3) - 1) & 1))) break;
         tc_fence_after();
-        const uint32_t sK = sbase + C::OFF_K + s * C::ATOMS * C::ATOM;
+        const uint32_t sK = sbase + C::OFF_KV + 2 * s * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::ATOM + (kk & 3) * 32;
@@ -180,128 +200,174 @@ __global__ void __launch_bounds__(kThreads, 1)
                  kk > 0, issue);
         }
         mma_commit(bar(F_S + s), issue);
-        return true;
-      };
-      bool ok = wall(F_Q, 0) && issue_s(0);
+      }
+      mma_commit(bar(F_FIN_S), issue);
+      mbar_drain(bar(F_FIN_S), 0);
+    } else {
+      // O += P(j) V_j once the softmax warps wrote P(j): packed bf16, key e
+      // at column e / 2 of buffer j % 3
       for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j & 1;
-        if (j + 1 < nkv && !(ok = issue_s(j + 1))) break;
-        if (!(ok = wall(F_P + s, (j >> 1) & 1))) break;
+        const int s = j % 3;
+        if (!(ok = wall(F_P + s, (j / 3) & 1))) break;
         tc_fence_after();
-        const uint32_t sV = sbase + C::OFF_V + s * C::ATOMS * C::ATOM;
+        const uint32_t sV = sbase + C::OFF_KV + (2 * s + 1) * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk)
           mma_ts(tm + C::TM_O, tm + C::TM_S + s * 128 + kk * 8, sdesc_sw128(sV + kk * 2048, C::ATOM, 1024), C::ID_PV,
                  (j > 0 || kk > 0) ? 1u : 0u, issue);
         mma_commit(bar(F_PV + s), issue);
-        mma_commit(bar(F_EMPTY + s), issue);
       }
-      mma_commit(bar(F_FINAL), issue);
-      mbar_drain(bar(F_FINAL), 0);
+      mma_commit(bar(F_FIN_O), issue);
+      mbar_drain(bar(F_FIN_O), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
+    // warps 2-5 take keys 0-63 of a tile, warps 6-9 keys 64-127; thread =
+    // query row.  The two halves of a row trade their maxima through shared
+    // memory once per tile (an OR-reducing named barrier, so an error ends
+    // every softmax thread's loop at the same tile).
+    const int hf = (warp - 2) >> 2;
     const int r = (warp & 3) * 32 + lane;
     const int64_t n = n0 + r;
     const bool row_ok = n < p.N;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c1 = p.scale * kLog2e;
-    float m_run = -INFINITY, l = 0.f;
+    const bool mvec = (p.M & 7) == 0;  // mask rows start 16-byte aligned
+    const uint16_t* mrow = p.mask + p.M * (row_ok ? n : 0);
+    uint32_t mk[MASK ? 32 : 1];
+    float m_run = -INFINITY, l = 0.f;  // l: this half's share of the row sum
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      const int s = j & 1;
+      const int s = j % 3;
       const int64_t m0 = (int64_t)j * C::BK;
-      ok = mbar_wait(bar(F_S + s), (j >> 1) & 1, abort_flag, err);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      const uint32_t tS = tm + lane_off + C::TM_S + s * 128;
-      // pass 1: the tile's row max (masked entries excluded)
-      float tmax = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t ra[32];
-        tmem_ld32(tS + c * 32, ra);
-        tmem_ld_wait(ra);
+      const int64_t mb = m0 + hf * 64;  // first key of this thread's columns
+      if (MASK) {
+        // this thread's 64 mask values (f16 pairs); entries past M read as 0
+        if (!row_ok) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int64_t m = m0 + c * 32 + e;
-          float x = __uint_as_float(ra[e]) * c1;
-          if (p.mask != nullptr && row_ok && m < p.M)
-            x = fmaf(__half2float(__ushort_as_half(p.mask[m + p.M * n])), kLog2e, x);
-          if ((p.causal && m > n) || m >= p.M || !row_ok) x = -INFINITY;
-          tmax = fmaxf(tmax, x);
+          for (int c = 0; c < 32; ++c) mk[c] = 0u;
+        } else if (mvec && mb + 64 <= p.M) {
+          const uint4* src = reinterpret_cast<const uint4*>(mrow + mb);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = __ldg(src + c);
+            mk[4 * c] = v.x;
+            mk[4 * c + 1] = v.y;
+            mk[4 * c + 2] = v.z;
+            mk[4 * c + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t lo = (mb + 2 * c < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c) : 0u;
+            const uint32_t hi = (mb + 2 * c + 1 < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c + 1) : 0u;
+            mk[c] = lo | (hi << 16);
+          }
         }
       }
+      const uint32_t tS = tm + lane_off + C::TM_S + s * 128;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(F_S + s), (j / 3) & 1, abort_flag, err));
+      float sv[64];
+      float hmax = -INFINITY;
+      if (got) {
+        tc_fence_after();
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tS + hf * 64, ra);
+        tmem_ld32(tS + hf * 64 + 32, rb);
+        tmem_ld_wait2(ra, rb);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) sv[e] = __uint_as_float(e < 32 ? ra[e] : rb[e - 32]) * c1;
+        if (MASK) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mk[c]));
+            sv[2 * c] = fmaf(mf.x, kLog2e, sv[2 * c]);
+            sv[2 * c + 1] = fmaf(mf.y, kLog2e, sv[2 * c + 1]);
+          }
+        }
+        // keys past the causal diagonal (top-left: key m > query n) or past
+        // M, and rows past N; only the diagonal tile and a ragged last tile
+        // (or query tile) have any
+        if ((p.causal && m0 + C::BK - 1 > n0) || m0 + C::BK > p.M || !row_ok) {
+          int64_t lim = 63;                              // last allowed column e (key mb + e)
+          if (p.causal && n - mb < lim) lim = n - mb;    // m <= n
+          if (p.M - 1 - mb < lim) lim = p.M - 1 - mb;    // m < M
+          if (!row_ok) lim = -1;
+          const int li = lim < -1 ? -1 : (int)lim;
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e > li) sv[e] = -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < 64; ++e) hmax = fmaxf(hmax, sv[e]);
+      }
+      mx[((j & 1) * 2 + hf) * C::BQ + r] = hmax;
+      if (named_bar_or(1, kSoftmaxThreads, !(got && ok))) {
+        ok = false;
+        break;
+      }
+      // (S(j) is in registers on both halves: P may now go over its columns)
+      const float tmax = fmaxf(hmax, mx[((j & 1) * 2 + (hf ^ 1)) * C::BQ + r]);
       float m_new = m_run, alpha = 1.f;
       if (tmax > m_run + kRescaleThreshold || (m_run == -INFINITY && tmax > -INFINITY)) {
         m_new = tmax;
         alpha = exp2f(m_run - m_new);  // 0 when m_run = -inf
       }
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      // pass 2: P = exp2(x - m), packed bf16 over the consumed S columns
-      float rsum = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t ra[32];
-        tmem_ld32(tS + c * 32, ra);
-        tmem_ld_wait(ra);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pe[2];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int64_t m = m0 + c * 32 + e + t;
-            float x = __uint_as_float(ra[e + t]) * c1;
-            if (p.mask != nullptr && row_ok && m < p.M)
-              x = fmaf(__half2float(__ushort_as_half(p.mask[m + p.M * n])), kLog2e, x);
-            if ((p.causal && m > n) || m >= p.M || !row_ok) x = -INFINITY;
-            pe[t] = ex2_approx(x - m_use);
-          }
-          const uint32_t packed = pack_bf16x2(pe[0], pe[1]);
-          // sum what the tensor core will see (the bf16-rounded P)
-          rsum += __uint_as_float(packed << 16) + __uint_as_float(packed & 0xffff0000u);
-          pk[e >> 1] = packed;
-        }
-        tmem_st16(tS + c * 16, pk);
-      }
-      l = l * alpha + rsum;
       const bool need = (m_new != m_run) && (m_run != -INFINITY) && j > 0;
       if (__any_sync(0xffffffffu, need)) {
-        // O holds sum_{j' < j} P V with the old max: rescale once PV(j-1) landed
-        const bool done = mbar_wait(bar(F_PV + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, err);
-        if (!__all_sync(0xffffffffu, done)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float f = need ? alpha : 1.f;
+        // O holds sum_{j' < j} P V with the old max: rescale this half's
+        // columns once PV(j-1) landed
+        const bool done = __all_sync(
+            0xffffffffu, mbar_wait(bar(F_PV + (j - 1) % 3), ((j - 1) / 3) & 1, abort_flag, err));
+        if (done) {
+          tc_fence_after();
+          const float f = need ? alpha : 1.f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t ra[32];
-          tmem_ld32(tm + lane_off + C::TM_O + c0, ra);
-          tmem_ld_wait(ra);
+          for (int c0 = 0; c0 < D / 2; c0 += 32) {
+            uint32_t ra[32];
+            tmem_ld32(tm + lane_off + C::TM_O + hf * (D / 2) + c0, ra);
+            tmem_ld_wait(ra);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ra[e] = __float_as_uint(__uint_as_float(ra[e]) * f);
-          tmem_st32(tm + lane_off + C::TM_O + c0, ra);
+            for (int e = 0; e < 32; ++e) ra[e] = __float_as_uint(__uint_as_float(ra[e]) * f);
+            tmem_st32(tm + lane_off + C::TM_O + hf * (D / 2) + c0, ra);
+          }
+        } else {
+          ok = false;
         }
       }
       m_run = m_new;
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      // P = exp2(x - m), packed bf16: key hf * 64 + e at column hf * 32 + e / 2
+      float rsum = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const uint32_t packed = pack_bf16x2(ex2_approx(sv[2 * c] - m_use), ex2_approx(sv[2 * c + 1] - m_use));
+        // sum what the tensor core will see (the bf16-rounded P)
+        rsum += __uint_as_float(packed << 16) + __uint_as_float(packed & 0xffff0000u);
+        pk[c] = packed;
+      }
+      tmem_st32(tS + hf * 32, pk);
+      l = l * alpha + rsum;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(F_P + s));
     }
-    // epilogue: O / l and the LSE
-    if (ok && nkv > 0) {
-      const bool done = mbar_wait(bar(F_PV + ((nkv - 1) & 1)), ((nkv - 1) >> 1) & 1, abort_flag, err);
-      if (__all_sync(0xffffffffu, done && !*abort_flag)) {
+    // epilogue: O / l (this half's columns) and the LSE; the halves' shares
+    // of l meet in the shared slot the last tile did not use
+    if (nkv > 0) {
+      const bool done = ok && __all_sync(0xffffffffu, mbar_wait(bar(F_PV + (nkv - 1) % 3), ((nkv - 1) / 3) & 1,
+                                                                abort_flag, err));
+      mx[((nkv & 1) * 2 + hf) * C::BQ + r] = l;
+      if (!named_bar_or(1, kSoftmaxThreads, !done || *abort_flag != 0u)) {
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = p.o + ((b * p.N + (row_ok ? n : 0)) * p.H + h) * D;
+        const float lt = l + mx[((nkv & 1) * 2 + (hf ^ 1)) * C::BQ + r];
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        __nv_bfloat16* orow = p.o + ((b * p.N + (row_ok ? n : 0)) * p.H + h) * D + hf * (D / 2);
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
           uint32_t ra[32];
-          tmem_ld32(tm + lane_off + C::TM_O + c0, ra);
+          tmem_ld32(tm + lane_off + C::TM_O + hf * (D / 2) + c0, ra);
           tmem_ld_wait(ra);
           if (row_ok) {
 #pragma unroll
@@ -315,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (row_ok) p.lse[(b * p.H + h) * p.N + n] = l > 0.f ? (m_run + log2f(l)) * kLn2 : INFINITY;
+        if (row_ok && hf == 0) p.lse[(b * p.H + h) * p.N + n] = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : INFINITY;
       }
     }
   }
@@ -338,7 +404,7 @@ bool make_map(CUtensorMap* map, const void* base, const cuuint64_t* dims, const 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool MASK>
 cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
   using C = FCfg<D>;
   CUtensorMap mq, mk, mv;
@@ -368,9 +434,10 @@ cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   const int64_t grid = ((pr.N + C::BQ - 1) / C::BQ) * pr.H * pr.B;
-  cudaError_t err = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t err =
+      cudaFuncSetAttribute(fwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  fwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, p);
+  fwd_tc_kernel<D, MASK><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, p);
   return cudaPeekAtLastError();
 }
 
@@ -385,7 +452,9 @@ bool forward_tc_supported(const Problem& p) {
 }
 
 cudaError_t launch_forward_tc(const Problem& p, void* o, float* lse, cudaStream_t s) {
-  return p.DK == 128 ? launch_d<128>(p, o, lse, s) : launch_d<64>(p, o, lse, s);
+  const bool m = p.mask != nullptr;
+  if (p.DK == 128) return m ? launch_d<128, true>(p, o, lse, s) : launch_d<128, false>(p, o, lse, s);
+  return m ? launch_d<64, true>(p, o, lse, s) : launch_d<64, false>(p, o, lse, s);
 }
 
 uint32_t take_error_fwd() {
