@@ -8,9 +8,12 @@
 // max m, sum l, unnormalised O, per key block); ggmlR attn_ref for the
 // additive mask (added after scaling) and for rows with no finite score.
 //
-// One CTA per (query tile of 128 rows, query head, batch), heavy causal
-// tiles first.  Q stays in shared memory; key/value tiles of 128 keys stream
-// through a three-stage TMA ring.  S = Q K_j^T lands in one of three
+// Work units of (query tile of 128 rows, query head, batch), heavy causal
+// tiles first; persistent CTAs, one per SM, walk them.  A unit's Q stays in
+// shared memory (the next unit's Q loads once the unit's last S MMA has read
+// it); key/value tiles of 128 keys stream through a three-stage TMA ring, and
+// ring stages, tensor-memory buffers and barrier phases count tiles across
+// units.  S = Q K_j^T lands in one of three
 // tensor-memory buffers, so the MMAs for the next tiles run while the softmax
 // warps turn tile j into P (bf16, written back over S) and the tensor core
 // then accumulates O += P V_j in tensor memory.  The running max is only
@@ -69,14 +72,16 @@ struct FCfg {
 };
 
 enum : int {
-  F_Q = 0,
-  F_FULL = 1,    // + j % 3: K_j and V_j landed
-  F_S = 4,       // + j % 3: S(j) landed
-  F_P = 7,       // + j % 3: softmax warps wrote P(j) (and rescaled O if they had to)
-  F_PV = 10,     // + j % 3: PV(j) finished (its stage, S buffer free; O holds tiles <= j)
+  F_Q = 0,       // phase k: unit k's Q landed
+  F_FULL = 1,    // + g % 3: K_g and V_g landed
+  F_S = 4,       // + g % 3: S(g) landed
+  F_P = 7,       // + g % 3: softmax warps wrote P(g) (and rescaled O if they had to)
+  F_PV = 10,     // + g % 3: PV(g) finished (its stage, S buffer free; O holds the unit's tiles <= g)
   F_FIN_S = 13,  // every S MMA finished
   F_FIN_O = 14,  // every PV MMA finished
-  F_COUNT = 15
+  F_QE = 15,     // phase k: unit k's S MMAs finished (Q free)
+  F_OE = 16,     // phase k: unit k's epilogue read O from tensor memory
+  F_COUNT = 17
 };
 
 struct FParams {
@@ -110,20 +115,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = (int)warp_id();
   const int lane = (int)lane_id();
 
-  // (query tile, head, batch); heavy (late) query tiles first under a causal mask
-  const int64_t q_tiles = (p.N + C::BQ - 1) / C::BQ;
-  const int64_t hb = p.H * p.B;
-  const int64_t qi = blockIdx.x / hb, rem = blockIdx.x % hb;
-  const int64_t b = rem / p.H, h = rem % p.H;
-  const int64_t qt = p.causal ? q_tiles - 1 - qi : qi;
-  const int64_t hkv = h / (p.H / p.Hkv);
-  const int64_t n0 = qt * C::BQ;
-  int64_t n_kv = (p.M + C::BK - 1) / C::BK;
-  if (p.causal) {
-    const int64_t last = (n0 + C::BQ - 1) / C::BK + 1;  // key tiles holding some m <= n
-    if (last < n_kv) n_kv = last;
-  }
-  const int nkv = (int)n_kv;
+  // work units: (query tile, head, batch), heavy (late) query tiles first
+  // under a causal mask.  Round k of the G CTAs takes units k G .. k G + G - 1,
+  // CTA c the c-th of them on even rounds and the (G-1-c)-th on odd rounds.
+  // (32-bit index arithmetic: the host guarantees units, N, M < 2^31.)
+  const int q_tiles = (int)((p.N + C::BQ - 1) / C::BQ);
+  const int hb = (int)(p.H * p.B);
+  const int n_units = q_tiles * hb;
+  const int H = (int)p.H, rk2 = (int)(p.H / p.Hkv), m_tiles = (int)((p.M + C::BK - 1) / C::BK);
+  struct Unit {
+    int h, b, hkv, n0, nkv;
+  };
+  auto unit_at = [&](int kk) {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    return G * kk + ((kk & 1) ? G - 1 - c : c);
+  };
+  auto unit_of = [&](int u) {
+    Unit x;
+    const int qi = u / hb, rem = u - qi * hb;
+    x.b = rem / H;
+    x.h = rem - x.b * H;
+    x.hkv = x.h / rk2;
+    const int qt = p.causal ? q_tiles - 1 - qi : qi;
+    x.n0 = qt * C::BQ;
+    int n_kv = m_tiles;
+    if (p.causal) {
+      const int last = (x.n0 + C::BQ - 1) / C::BK + 1;  // key tiles holding some m <= n
+      if (last < n_kv) n_kv = last;
+    }
+    x.nkv = n_kv;  // >= 1: key tile 0 holds m = 0 <= n
+    return x;
+  };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
@@ -136,6 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(F_FIN_S), 1);
     mbar_init(bar(F_FIN_O), 1);
+    mbar_init(bar(F_QE), 1);
+    mbar_init(bar(F_OE), kSoftmaxThreads);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -149,28 +173,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Q once; K_j, V_j into stage j % 3 once PV(j-3) is done with it
+    // Per unit: K_g, V_g of its first tile, its Q (once the previous unit's
+    // S MMAs are done with theirs), then the other tiles' K, V.  K_g, V_g go
+    // into stage g % 3 once PV(g-3) is done with it; g counts tiles across
+    // units.
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
-      mbar_arrive_expect_tx(bar(F_Q), C::TILE);
-      for (int a = 0; a < C::ATOMS; ++a)
-        tma_load_3d(sbase + C::OFF_Q + a * C::ATOM, &tmQ, bar(F_Q), a * 64, (int)n0, (int)(b * p.H + h));
-      int issued = 0;
-      const int kvrow = (int)(b * p.Hkv + hkv);
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j % 3;
-        if (j >= 3 && !mbar_wait(bar(F_PV + s), ((j / 3) - 1) & 1, abort_flag, err)) break;
-        mbar_arrive_expect_tx(bar(F_FULL + s), 2 * C::TILE);
-        const uint32_t sk = sbase + C::OFF_KV + 2 * s * C::TILE;
-        for (int a = 0; a < C::ATOMS; ++a) {
-          tma_load_3d(sk + a * C::ATOM, &tmK, bar(F_FULL + s), a * 64, j * C::BK, kvrow);
-          tma_load_3d(sk + C::TILE + a * C::ATOM, &tmV, bar(F_FULL + s), a * 64, j * C::BK, kvrow);
+      int g = 0, k = 0, issued = 0, q_issued = 0;
+      bool ok = true;
+      for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
+        const Unit x = unit_of(u);
+        const int kvrow = x.b * (int)p.Hkv + x.hkv;
+        for (int j = 0; j < x.nkv; ++j, ++g) {
+          const int s = g % 3;
+          if (g >= 3 && !(ok = mbar_wait(bar(F_PV + s), ((g / 3) - 1) & 1, abort_flag, err))) break;
+          mbar_arrive_expect_tx(bar(F_FULL + s), 2 * C::TILE);
+          const uint32_t sk = sbase + C::OFF_KV + 2 * s * C::TILE;
+          for (int a = 0; a < C::ATOMS; ++a) {
+            tma_load_3d(sk + a * C::ATOM, &tmK, bar(F_FULL + s), a * 64, j * C::BK, kvrow);
+            tma_load_3d(sk + C::TILE + a * C::ATOM, &tmV, bar(F_FULL + s), a * 64, j * C::BK, kvrow);
+          }
+          ++issued;
+          if (j == 0) {
+            if (k > 0 && !(ok = mbar_wait(bar(F_QE), (k - 1) & 1, abort_flag, err))) break;
+            mbar_arrive_expect_tx(bar(F_Q), C::TILE);
+            for (int a = 0; a < C::ATOMS; ++a)
+              tma_load_3d(sbase + C::OFF_Q + a * C::ATOM, &tmQ, bar(F_Q), a * 64, x.n0, x.b * H + x.h);
+            ++q_issued;
+          }
         }
-        ++issued;
       }
-      mbar_drain(bar(F_Q), 0);
+      if (q_issued > 0) mbar_drain(bar(F_Q), (q_issued - 1) & 1);
       for (int j = issued > 3 ? issued - 3 : 0; j < issued; ++j) mbar_drain(bar(F_FULL + j % 3), (j / 3) & 1);
     }
   } else if (warp == 1 || warp == 10) {
@@ -183,39 +218,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = true;
     if (warp == 1) {
-      // S(j) = Q K_j^T into buffer j % 3 once K_j landed and PV(j-3) is done
-      // with the buffer's P
+      // S(g) = Q K_g^T into buffer g % 3 once K_g landed and PV(g-3) is done
+      // with the buffer's P; after a unit's last S, its Q is free
       const uint32_t sQ = sbase + C::OFF_Q;
-      ok = wall(F_Q, 0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % 3;
-        if (!(ok = wall(F_FULL + s, (j / 3) & 1))) break;
-        if (j >= 3 && !(ok = wall(F_PV + s, ((j / 3) - 1) & 1))) break;
-        tc_fence_after();
-        const uint32_t sK = sbase + C::OFF_KV + 2 * s * C::TILE;
+      int g = 0, k = 0;
+      for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
+        const int nkv = unit_of(u).nkv;
+        if (!(ok = wall(F_Q, k & 1))) break;
+        for (int j = 0; j < nkv; ++j, ++g) {
+          const int s = g % 3;
+          if (!(ok = wall(F_FULL + s, (g / 3) & 1))) break;
+          if (g >= 3 && !(ok = wall(F_PV + s, ((g / 3) - 1) & 1))) break;
+          tc_fence_after();
+          const uint32_t sK = sbase + C::OFF_KV + 2 * s * C::TILE;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::ATOM + (kk & 3) * 32;
-          mma_ss(tm + C::TM_S + s * 128, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), C::ID_S,
-                 kk > 0, issue);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::ATOM + (kk & 3) * 32;
+            mma_ss(tm + C::TM_S + s * 128, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024),
+                   C::ID_S, kk > 0, issue);
+          }
+          mma_commit(bar(F_S + s), issue);
         }
-        mma_commit(bar(F_S + s), issue);
+        mma_commit(bar(F_QE), issue);
       }
       mma_commit(bar(F_FIN_S), issue);
       mbar_drain(bar(F_FIN_S), 0);
     } else {
-      // O += P(j) V_j once the softmax warps wrote P(j): packed bf16, key e
-      // at column e / 2 of buffer j % 3
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % 3;
-        if (!(ok = wall(F_P + s, (j / 3) & 1))) break;
-        tc_fence_after();
-        const uint32_t sV = sbase + C::OFF_KV + (2 * s + 1) * C::TILE;
+      // O += P(g) V_g once the softmax warps wrote P(g): packed bf16, key e
+      // at column e / 2 of buffer g % 3; a unit's first product waits for
+      // the previous unit's epilogue to have read O
+      int g = 0, k = 0;
+      for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
+        const int nkv = unit_of(u).nkv;
+        for (int j = 0; j < nkv; ++j, ++g) {
+          const int s = g % 3;
+          if (!(ok = wall(F_P + s, (g / 3) & 1))) break;
+          if (j == 0 && k > 0 && !(ok = wall(F_OE, (k - 1) & 1))) break;
+          tc_fence_after();
+          const uint32_t sV = sbase + C::OFF_KV + (2 * s + 1) * C::TILE;
 #pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk)
-          mma_ts(tm + C::TM_O, tm + C::TM_S + s * 128 + kk * 8, sdesc_sw128(sV + kk * 2048, C::ATOM, 1024), C::ID_PV,
-                 (j > 0 || kk > 0) ? 1u : 0u, issue);
-        mma_commit(bar(F_PV + s), issue);
+          for (int kk = 0; kk < C::BK / 16; ++kk)
+            mma_ts(tm + C::TM_O, tm + C::TM_S + s * 128 + kk * 8, sdesc_sw128(sV + kk * 2048, C::ATOM, 1024),
+                   C::ID_PV, (j > 0 || kk > 0) ? 1u : 0u, issue);
+          mma_commit(bar(F_PV + s), issue);
+        }
       }
       mma_commit(bar(F_FIN_O), issue);
       mbar_drain(bar(F_FIN_O), 0);
@@ -228,161 +274,174 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every softmax thread's loop at the same tile).
     const int hf = (warp - 2) >> 2;
     const int r = (warp & 3) * 32 + lane;
-    const int64_t n = n0 + r;
-    const bool row_ok = n < p.N;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c1 = p.scale * kLog2e;
     const bool mvec = (p.M & 7) == 0;  // mask rows start 16-byte aligned
-    const uint16_t* mrow = p.mask + p.M * (row_ok ? n : 0);
     uint32_t mk[MASK ? 32 : 1];
-    float m_run = -INFINITY, l = 0.f;  // l: this half's share of the row sum
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int s = j % 3;
-      const int64_t m0 = (int64_t)j * C::BK;
-      const int64_t mb = m0 + hf * 64;  // first key of this thread's columns
-      if (MASK) {
-        // this thread's 64 mask values (f16 pairs); entries past M read as 0
-        if (!row_ok) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) mk[c] = 0u;
-        } else if (mvec && mb + 64 <= p.M) {
-          const uint4* src = reinterpret_cast<const uint4*>(mrow + mb);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 v = __ldg(src + c);
-            mk[4 * c] = v.x;
-            mk[4 * c + 1] = v.y;
-            mk[4 * c + 2] = v.z;
-            mk[4 * c + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const uint32_t lo = (mb + 2 * c < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c) : 0u;
-            const uint32_t hi = (mb + 2 * c + 1 < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c + 1) : 0u;
-            mk[c] = lo | (hi << 16);
-          }
-        }
-      }
-      const uint32_t tS = tm + lane_off + C::TM_S + s * 128;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(F_S + s), (j / 3) & 1, abort_flag, err));
-      float sv[64];
-      float hmax = -INFINITY;
-      if (got) {
-        tc_fence_after();
-        uint32_t ra[32], rb[32];
-        tmem_ld32(tS + hf * 64, ra);
-        tmem_ld32(tS + hf * 64 + 32, rb);
-        tmem_ld_wait2(ra, rb);
-#pragma unroll
-        for (int e = 0; e < 64; ++e) sv[e] = __uint_as_float(e < 32 ? ra[e] : rb[e - 32]) * c1;
+    int g = 0, k = 0;
+    for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
+      const Unit x = unit_of(u);
+      const int64_t n = (int64_t)x.n0 + r;
+      const bool row_ok = n < p.N;
+      const uint16_t* mrow = p.mask + p.M * (row_ok ? n : 0);
+      float m_run = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+      for (int j = 0; j < x.nkv; ++j, ++g) {
+        const int s = g % 3;
+        const int64_t m0 = (int64_t)j * C::BK;
+        const int64_t mb = m0 + hf * 64;  // first key of this thread's columns
         if (MASK) {
+          // this thread's 64 mask values (f16 pairs); entries past M read as 0
+          if (!row_ok) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mk[c]));
-            sv[2 * c] = fmaf(mf.x, kLog2e, sv[2 * c]);
-            sv[2 * c + 1] = fmaf(mf.y, kLog2e, sv[2 * c + 1]);
-          }
-        }
-        // keys past the causal diagonal (top-left: key m > query n) or past
-        // M, and rows past N; only the diagonal tile and a ragged last tile
-        // (or query tile) have any
-        if ((p.causal && m0 + C::BK - 1 > n0) || m0 + C::BK > p.M || !row_ok) {
-          int64_t lim = 63;                              // last allowed column e (key mb + e)
-          if (p.causal && n - mb < lim) lim = n - mb;    // m <= n
-          if (p.M - 1 - mb < lim) lim = p.M - 1 - mb;    // m < M
-          if (!row_ok) lim = -1;
-          const int li = lim < -1 ? -1 : (int)lim;
+            for (int c = 0; c < 32; ++c) mk[c] = 0u;
+          } else if (mvec && mb + 64 <= p.M) {
+            const uint4* src = reinterpret_cast<const uint4*>(mrow + mb);
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (e > li) sv[e] = -INFINITY;
-        }
+            for (int c = 0; c < 8; ++c) {
+              const uint4 v = __ldg(src + c);
+              mk[4 * c] = v.x;
+              mk[4 * c + 1] = v.y;
+              mk[4 * c + 2] = v.z;
+              mk[4 * c + 3] = v.w;
+            }
+          } else {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) hmax = fmaxf(hmax, sv[e]);
-      }
-      mx[((j & 1) * 2 + hf) * C::BQ + r] = hmax;
-      if (named_bar_or(1, kSoftmaxThreads, !(got && ok))) {
-        ok = false;
-        break;
-      }
-      // (S(j) is in registers on both halves: P may now go over its columns)
-      const float tmax = fmaxf(hmax, mx[((j & 1) * 2 + (hf ^ 1)) * C::BQ + r]);
-      float m_new = m_run, alpha = 1.f;
-      if (tmax > m_run + kRescaleThreshold || (m_run == -INFINITY && tmax > -INFINITY)) {
-        m_new = tmax;
-        alpha = exp2f(m_run - m_new);  // 0 when m_run = -inf
-      }
-      const bool need = (m_new != m_run) && (m_run != -INFINITY) && j > 0;
-      if (__any_sync(0xffffffffu, need)) {
-        // O holds sum_{j' < j} P V with the old max: rescale this half's
-        // columns once PV(j-1) landed
-        const bool done = __all_sync(
-            0xffffffffu, mbar_wait(bar(F_PV + (j - 1) % 3), ((j - 1) / 3) & 1, abort_flag, err));
-        if (done) {
-          tc_fence_after();
-          const float f = need ? alpha : 1.f;
-#pragma unroll 1
-          for (int c0 = 0; c0 < D / 2; c0 += 32) {
-            uint32_t ra[32];
-            tmem_ld32(tm + lane_off + C::TM_O + hf * (D / 2) + c0, ra);
-            tmem_ld_wait(ra);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ra[e] = __float_as_uint(__uint_as_float(ra[e]) * f);
-            tmem_st32(tm + lane_off + C::TM_O + hf * (D / 2) + c0, ra);
-          }
-        } else {
-          ok = false;
-        }
-      }
-      m_run = m_new;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      // P = exp2(x - m), packed bf16: key hf * 64 + e at column hf * 32 + e / 2
-      float rsum = 0.f;
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const uint32_t packed = pack_bf16x2(ex2_approx(sv[2 * c] - m_use), ex2_approx(sv[2 * c + 1] - m_use));
-        // sum what the tensor core will see (the bf16-rounded P)
-        rsum += __uint_as_float(packed << 16) + __uint_as_float(packed & 0xffff0000u);
-        pk[c] = packed;
-      }
-      tmem_st32(tS + hf * 32, pk);
-      l = l * alpha + rsum;
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(F_P + s));
-    }
-    // epilogue: O / l (this half's columns) and the LSE; the halves' shares
-    // of l meet in the shared slot the last tile did not use
-    if (nkv > 0) {
-      const bool done = ok && __all_sync(0xffffffffu, mbar_wait(bar(F_PV + (nkv - 1) % 3), ((nkv - 1) / 3) & 1,
-                                                                abort_flag, err));
-      mx[((nkv & 1) * 2 + hf) * C::BQ + r] = l;
-      if (!named_bar_or(1, kSoftmaxThreads, !done || *abort_flag != 0u)) {
-        tc_fence_after();
-        const float lt = l + mx[((nkv & 1) * 2 + (hf ^ 1)) * C::BQ + r];
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        __nv_bfloat16* orow = p.o + ((b * p.N + (row_ok ? n : 0)) * p.H + h) * D + hf * (D / 2);
-#pragma unroll 1
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          uint32_t ra[32];
-          tmem_ld32(tm + lane_off + C::TM_O + hf * (D / 2) + c0, ra);
-          tmem_ld_wait(ra);
-          if (row_ok) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(ra[e]) * inv, __uint_as_float(ra[e + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(ra[e + 2]) * inv, __uint_as_float(ra[e + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(ra[e + 4]) * inv, __uint_as_float(ra[e + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(ra[e + 6]) * inv, __uint_as_float(ra[e + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + c0 + e) = v;
+            for (int c = 0; c < 32; ++c) {
+              const uint32_t lo = (mb + 2 * c < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c) : 0u;
+              const uint32_t hi = (mb + 2 * c + 1 < p.M) ? (uint32_t)__ldg(mrow + mb + 2 * c + 1) : 0u;
+              mk[c] = lo | (hi << 16);
             }
           }
         }
-        if (row_ok && hf == 0) p.lse[(b * p.H + h) * p.N + n] = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : INFINITY;
+        const uint32_t tS = tm + lane_off + C::TM_S + s * 128;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(bar(F_S + s), (g / 3) & 1, abort_flag, err));
+        float sv[64];
+        float hmax = -INFINITY;
+        if (got) {
+          tc_fence_after();
+          uint32_t ra[32], rb[32];
+          tmem_ld32(tS + hf * 64, ra);
+          tmem_ld32(tS + hf * 64 + 32, rb);
+          tmem_ld_wait2(ra, rb);
+#pragma unroll
+          for (int e = 0; e < 64; ++e) sv[e] = __uint_as_float(e < 32 ? ra[e] : rb[e - 32]) * c1;
+          if (MASK) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float2 mf = __half22float2(*reinterpret_cast<const __half2*>(&mk[c]));
+              sv[2 * c] = fmaf(mf.x, kLog2e, sv[2 * c]);
+              sv[2 * c + 1] = fmaf(mf.y, kLog2e, sv[2 * c + 1]);
+            }
+          }
+          // keys past the causal diagonal (top-left: key m > query n) or past
+          // M, and rows past N; only the diagonal tile and a ragged last tile
+          // (or query tile) have any
+          if ((p.causal && m0 + C::BK - 1 > x.n0) || m0 + C::BK > p.M || !row_ok) {
+            int64_t lim = 63;                              // last allowed column e (key mb + e)
+            if (p.causal && n - mb < lim) lim = n - mb;    // m <= n
+            if (p.M - 1 - mb < lim) lim = p.M - 1 - mb;    // m < M
+            if (!row_ok) lim = -1;
+            const int li = lim < -1 ? -1 : (int)lim;
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (e > li) sv[e] = -INFINITY;
+          }
+#pragma unroll
+          for (int e = 0; e < 64; ++e) hmax = fmaxf(hmax, sv[e]);
+        }
+        mx[((g & 1) * 2 + hf) * C::BQ + r] = hmax;
+        if (named_bar_or(1, kSoftmaxThreads, !(got && ok))) {
+          ok = false;
+          break;
+        }
+        // (S(g) is in registers on both halves: P may now go over its columns)
+        const float tmax = fmaxf(hmax, mx[((g & 1) * 2 + (hf ^ 1)) * C::BQ + r]);
+        float m_new = m_run, alpha = 1.f;
+        if (tmax > m_run + kRescaleThreshold || (m_run == -INFINITY && tmax > -INFINITY)) {
+          m_new = tmax;
+          alpha = exp2f(m_run - m_new);  // 0 when m_run = -inf
+        }
+        const bool need = (m_new != m_run) && (m_run != -INFINITY) && j > 0;
+        if (__any_sync(0xffffffffu, need)) {
+          // O holds the unit's sum_{j' < j} P V with the old max: rescale this
+          // half's columns once PV(g-1) landed
+          const bool done = __all_sync(
+              0xffffffffu, mbar_wait(bar(F_PV + (g - 1) % 3), ((g - 1) / 3) & 1, abort_flag, err));
+          if (done) {
+            tc_fence_after();
+            const float f = need ? alpha : 1.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D / 2; c0 += 32) {
+              uint32_t ra[32];
+              tmem_ld32(tm + lane_off + C::TM_O + hf * (D / 2) + c0, ra);
+              tmem_ld_wait(ra);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ra[e] = __float_as_uint(__uint_as_float(ra[e]) * f);
+              tmem_st32(tm + lane_off + C::TM_O + hf * (D / 2) + c0, ra);
+            }
+          } else {
+            ok = false;
+          }
+        }
+        m_run = m_new;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        // P = exp2(x - m), packed bf16: key hf * 64 + e at column hf * 32 + e / 2
+        float rsum = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const uint32_t packed = pack_bf16x2(ex2_approx(sv[2 * c] - m_use), ex2_approx(sv[2 * c + 1] - m_use));
+          // sum what the tensor core will see (the bf16-rounded P)
+          rsum += __uint_as_float(packed << 16) + __uint_as_float(packed & 0xffff0000u);
+          pk[c] = packed;
+        }
+        tmem_st32(tS + hf * 32, pk);
+        l = l * alpha + rsum;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(F_P + s));
       }
+      // epilogue: O / l (this half's columns) and the LSE.  The halves' shares
+      // of l meet in the last tile's shared slot: the first barrier below
+      // lets both halves finish reading the maxima there, the second
+      // publishes l.  Then O has been read: the next unit's first PV may
+      // overwrite it.  (A warp whose wait failed reaches the first barrier
+      // too, so every softmax thread leaves together.)
+      const int G = g - 1;  // the unit's last tile
+      const bool done =
+          ok && __all_sync(0xffffffffu, mbar_wait(bar(F_PV + G % 3), (G / 3) & 1, abort_flag, err));
+      if (named_bar_or(1, kSoftmaxThreads, !done || *abort_flag != 0u)) {
+        ok = false;
+        break;
+      }
+      mx[((G & 1) * 2 + hf) * C::BQ + r] = l;
+      named_bar_sync(1, kSoftmaxThreads);
+      tc_fence_after();
+      const float lt = l + mx[((G & 1) * 2 + (hf ^ 1)) * C::BQ + r];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      __nv_bfloat16* orow = p.o + (((int64_t)x.b * p.N + (row_ok ? n : 0)) * p.H + x.h) * D + hf * (D / 2);
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t ra[32];
+        tmem_ld32(tm + lane_off + C::TM_O + hf * (D / 2) + c0, ra);
+        tmem_ld_wait(ra);
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(ra[e]) * inv, __uint_as_float(ra[e + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(ra[e + 2]) * inv, __uint_as_float(ra[e + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(ra[e + 4]) * inv, __uint_as_float(ra[e + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(ra[e + 6]) * inv, __uint_as_float(ra[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c0 + e) = v;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(F_OE));
+      if (row_ok && hf == 0)
+        p.lse[((int64_t)x.b * p.H + x.h) * p.N + n] = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : INFINITY;
     }
   }
 
@@ -433,7 +492,12 @@ cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
   p.mask = pr.mask;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
-  const int64_t grid = ((pr.N + C::BQ - 1) / C::BQ) * pr.H * pr.B;
+  // persistent: one CTA per SM (each owns the SM's tensor memory), walking units
+  const int64_t units = ((pr.N + C::BQ - 1) / C::BQ) * pr.H * pr.B;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  const int64_t grid = units < sms ? units : sms;
   cudaError_t err =
       cudaFuncSetAttribute(fwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
