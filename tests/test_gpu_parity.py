@@ -45,6 +45,9 @@ SMALL = [
     ("simt_f32_mask", 2, 2, 2, 33, 65, 64, 64, "f32", False, "random"),
     ("simt_bf16_odd", 1, 2, 1, 33, 47, 40, 24, "bf16", False, "random"),
     ("simt_f32_wide", 1, 1, 1, 20, 30, 256, 200, "f32", True, "none"),
+    # the pages' packing shape: widths below one 16-byte chunk, DK != DV
+    ("simt_f32_dk3_dv5", 2, 4, 2, 37, 29, 3, 5, "f32", False, "random"),
+    ("simt_bf16_dk3_dv5", 1, 2, 1, 33, 20, 3, 5, "bf16", True, "none"),
 ]
 
 
