@@ -414,7 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A unit's first global reads (this thread's LSE, its half row of O for
     // D_i, its first mask chunk) are issued before the previous unit's
     // epilogue, so their latency hides behind it.
-    uint4 ov[D / 16];
+    constexpr int CPH = D / 16;      // 16-byte chunks per half row
+    constexpr int RPI = 32 / CPH;    // rows per load instruction
+    uint4 ov[CPH];
     float lse_next = 0.f, di_next = 0.f;
     uint32_t mk[32];
     // (loads only, from a valid row: nothing here consumes a loaded value,
@@ -426,9 +428,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       lse_next = ld_global_nc_f32(p.lse + (y.b * p.H + y.h) * p.N + ny);
       if (!FUSE_D) di_next = p.di[(y.b * p.H + y.h) * p.N + ny];
       if (FUSE_D) {
-        const uint4* orow = reinterpret_cast<const uint4*>(p.o + ((y.b * p.N + ny) * p.H + y.h) * D + hf * (D / 2));
+        // whole half rows per instruction: instruction i, lane l reads chunk
+        // l % CPH of (this warp's) row i * RPI + l / CPH, so a row is full
+        // cache lines rather than one sector per thread
 #pragma unroll
-        for (int c = 0; c < D / 16; ++c) ov[c] = ld_global_nc_v4(orow + c);
+        for (int i = 0; i < CPH; ++i) {
+          const int64_t nr = (int64_t)y.n0 + (warp & 3) * 32 + i * RPI + lane / CPH;
+          const int64_t nc = nr < p.N ? nr : p.N - 1;
+          ov[i] = ld_global_nc_v4(reinterpret_cast<const uint4*>(p.o + ((y.b * p.N + nc) * p.H + y.h) * D +
+                                                                 hf * (D / 2) + (lane % CPH) * 8));
+        }
       }
     };
     int g = 0, k = 0;
@@ -452,12 +461,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             return __uint_as_float(a << 16) * __uint_as_float(b << 16) +
                    __uint_as_float(a & 0xffff0000u) * __uint_as_float(b & 0xffff0000u);
           };
+          // chunk l % CPH of row i * RPI + l / CPH (as loaded), against the
+          // same chunk of dO from the swizzled tile; the CPH lanes of a row
+          // sum by shuffles, then each thread takes its own row's sum
+          const int c = lane % CPH;
+          const int e = hf * (D / 2) + 8 * c;  // first column of the 16-byte chunk
 #pragma unroll
-          for (int c = 0; c < D / 16; ++c) {
-            const int e = hf * (D / 2) + 8 * c;  // first column of the 16-byte chunk
-            const uint4 dv = ld_shared_v4(sbase + C::OFF_DO + (uint32_t)(e / 64) * C::ATOM + r * 128 +
-                                          ((((e % 64) / 8) ^ (r & 7)) << 4));
-            part += dot2(dv.x, ov[c].x) + dot2(dv.y, ov[c].y) + dot2(dv.z, ov[c].z) + dot2(dv.w, ov[c].w);
+          for (int i = 0; i < CPH; ++i) {
+            const int rr = (warp & 3) * 32 + i * RPI + lane / CPH;
+            const uint4 dv = ld_shared_v4(sbase + C::OFF_DO + (uint32_t)(e / 64) * C::ATOM + rr * 128 +
+                                          ((((e % 64) / 8) ^ (rr & 7)) << 4));
+            float q = dot2(dv.x, ov[i].x) + dot2(dv.y, ov[i].y) + dot2(dv.z, ov[i].z) + dot2(dv.w, ov[i].w);
+#pragma unroll
+            for (int o = CPH / 2; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+            const float mine = __shfl_sync(0xffffffffu, q, (lane % RPI) * CPH);
+            if (i == lane / RPI) part = mine;
           }
         }
         dpart[hf * C::BQ + r] = row_ok ? part : 0.f;
