@@ -81,7 +81,8 @@ enum : int {
   F_FIN_O = 14,  // every PV MMA finished
   F_QE = 15,     // phase k: unit k's S MMAs finished (Q free)
   F_OE = 16,     // phase k: unit k's epilogue read O from tensor memory
-  F_COUNT = 17
+  F_STG = 17,    // phase k: unit k's O is staged in shared memory
+  F_COUNT = 18
 };
 
 struct FParams {
@@ -96,7 +97,8 @@ struct FParams {
 template <int D, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmOut,
+                  const FParams p) {
   using C = FCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -110,6 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
   float* mx = reinterpret_cast<float*>(smem + C::OFF_MX);
+  // units whose staged O the bulk stores have read (the staging is the key
+  // tile of the unit's last stage)
+  uint32_t* o_cnt = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 8);
   uint32_t* err = &g_err_fwd;
 
   const int warp = (int)warp_id();
@@ -149,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
+    *o_cnt = 0u;
     mbar_init(bar(F_Q), 1);
     for (int s = 0; s < 3; ++s) {
       mbar_init(bar(F_FULL + s), 1);
@@ -160,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(F_FIN_O), 1);
     mbar_init(bar(F_QE), 1);
     mbar_init(bar(F_OE), kSoftmaxThreads);
+    mbar_init(bar(F_STG), kSoftmaxThreads);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -176,12 +183,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Per unit: K_g, V_g of its first tile, its Q (once the previous unit's
     // S MMAs are done with theirs), then the other tiles' K, V.  K_g, V_g go
     // into stage g % 3 once PV(g-3) is done with it; g counts tiles across
-    // units.
+    // units.  A unit's epilogue stages O in the key tile of its last stage
+    // G % 3, so K_{G+3} also waits for that unit's bulk stores to read it.
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmOut);
       int g = 0, k = 0, issued = 0, q_issued = 0;
+      int stG[3] = {-8, -8, -8}, stK[3] = {0, 0, 0};  // last tile and index of the latest units
       bool ok = true;
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
         const Unit x = unit_of(u);
@@ -189,6 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < x.nkv; ++j, ++g) {
           const int s = g % 3;
           if (g >= 3 && !(ok = mbar_wait(bar(F_PV + s), ((g / 3) - 1) & 1, abort_flag, err))) break;
+#pragma unroll
+          for (int i = 0; i < 3; ++i)
+            if (ok && stG[i] + 3 == g) ok = counter_wait(o_cnt, (uint32_t)(stK[i] + 1), abort_flag, err);
+          if (!ok) break;
+          fence_proxy_async_smem();
           mbar_arrive_expect_tx(bar(F_FULL + s), 2 * C::TILE);
           const uint32_t sk = sbase + C::OFF_KV + 2 * s * C::TILE;
           for (int a = 0; a < C::ATOMS; ++a) {
@@ -204,6 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++q_issued;
           }
         }
+        stG[k % 3] = g - 1;
+        stK[k % 3] = k;
       }
       if (q_issued > 0) mbar_drain(bar(F_Q), (q_issued - 1) & 1);
       for (int j = issued > 3 ? issued - 3 : 0; j < issued; ++j) mbar_drain(bar(F_FULL + j % 3), (j / 3) & 1);
@@ -246,10 +263,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // O += P(g) V_g once the softmax warps wrote P(g): packed bf16, key e
       // at column e / 2 of buffer g % 3; a unit's first product waits for
-      // the previous unit's epilogue to have read O
+      // the previous unit's epilogue to have read O.  After a unit's last
+      // product, once the softmax warps staged O/l, this warp writes it out
+      // with bulk tensor stores and releases the staging once they read it.
       int g = 0, k = 0;
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
-        const int nkv = unit_of(u).nkv;
+        const Unit x = unit_of(u);
+        const int nkv = x.nkv;
         for (int j = 0; j < nkv; ++j, ++g) {
           const int s = g % 3;
           if (!(ok = wall(F_P + s, (g / 3) & 1))) break;
@@ -262,7 +282,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                    C::ID_PV, (j > 0 || kk > 0) ? 1u : 0u, issue);
           mma_commit(bar(F_PV + s), issue);
         }
+        if (!ok) break;
+        if (!(ok = wall(F_STG, k & 1))) break;
+        if (lane == 0) {
+          const uint32_t st = sbase + C::OFF_KV + 2 * ((g - 1) % 3) * C::TILE;  // key tile of the last stage
+          for (int a = 0; a < C::ATOMS; ++a) tma_store_4d(&tmOut, st + a * C::ATOM, a * 64, x.h, x.n0, x.b);
+          bulk_commit_group();
+          bulk_wait_read_all();
+          counter_bump(o_cnt);
+        }
+        __syncwarp();
       }
+      if (lane == 0) bulk_wait_read_all();  // (every group was waited for above; kept for an early exit)
       mma_commit(bar(F_FIN_O), issue);
       mbar_drain(bar(F_FIN_O), 0);
     }
@@ -420,26 +451,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float lt = l + mx[((G & 1) * 2 + (hf ^ 1)) * C::BQ + r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      __nv_bfloat16* orow = p.o + (((int64_t)x.b * p.N + (row_ok ? n : 0)) * p.H + x.h) * D + hf * (D / 2);
+      // O / l in bf16, staged in the key tile of the last stage as 64-column
+      // atoms of 128-byte swizzled rows (that stage's products are done; the
+      // producer holds K_{G+3} until the stores have read it); the PV issuer
+      // writes it out, clipping rows past N
+      const uint32_t st = sbase + C::OFF_KV + 2 * (G % 3) * C::TILE;
 #pragma unroll 1
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
         uint32_t ra[32];
         tmem_ld32(tm + lane_off + C::TM_O + hf * (D / 2) + c0, ra);
         tmem_ld_wait(ra);
-        if (row_ok) {
+        const int col = hf * (D / 2) + c0;  // first of these 32 columns
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(ra[e]) * inv, __uint_as_float(ra[e + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(ra[e + 2]) * inv, __uint_as_float(ra[e + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(ra[e + 4]) * inv, __uint_as_float(ra[e + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(ra[e + 6]) * inv, __uint_as_float(ra[e + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c0 + e) = v;
-          }
+        for (int e = 0; e < 32; e += 8) {
+          const int ch = ((col + e) % 64) / 8;  // 16-byte chunk within the 128-byte row
+          st_shared_v4(st + (uint32_t)((col + e) / 64) * C::ATOM + r * 128 + ((ch ^ (r & 7)) << 4),
+                       pack_bf16x2(__uint_as_float(ra[e]) * inv, __uint_as_float(ra[e + 1]) * inv),
+                       pack_bf16x2(__uint_as_float(ra[e + 2]) * inv, __uint_as_float(ra[e + 3]) * inv),
+                       pack_bf16x2(__uint_as_float(ra[e + 4]) * inv, __uint_as_float(ra[e + 5]) * inv),
+                       pack_bf16x2(__uint_as_float(ra[e + 6]) * inv, __uint_as_float(ra[e + 7]) * inv));
         }
       }
+      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(F_OE));
+      mbar_arrive(bar(F_STG));
       if (row_ok && hf == 0)
         p.lse[((int64_t)x.b * p.H + x.h) * p.N + n] = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : INFINITY;
     }
@@ -463,10 +499,20 @@ bool make_map(CUtensorMap* map, const void* base, const cuuint64_t* dims, const 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map4(CUtensorMap* map, const void* base, const cuuint64_t* dims, const cuuint64_t* strides,
+               const cuuint32_t* box) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, bool MASK>
 cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
   using C = FCfg<D>;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const cuuint64_t e = 2;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
@@ -480,6 +526,14 @@ cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
     const cuuint32_t box[3] = {64, (cuuint32_t)C::BK, 1};
     if (!make_map(&mk, pr.k, dims, str, box)) return cudaErrorInvalidValue;
     if (!make_map(&mv, pr.v, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    // O [DV,H,N,B]: rows n of one head are H*DV elements apart; stored in
+    // 64-column boxes of 128 rows
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)pr.H, (cuuint64_t)pr.N, (cuuint64_t)pr.B};
+    const cuuint64_t str[3] = {D * e, (cuuint64_t)pr.H * D * e, (cuuint64_t)pr.N * pr.H * D * e};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)C::BQ, 1};
+    if (!make_map4(&mo, o, dims, str, box)) return cudaErrorInvalidValue;
   }
   FParams p;
   p.B = pr.B;
@@ -501,7 +555,7 @@ cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
   cudaError_t err =
       cudaFuncSetAttribute(fwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  fwd_tc_kernel<D, MASK><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, p);
+  fwd_tc_kernel<D, MASK><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, p);
   return cudaPeekAtLastError();
 }
 
