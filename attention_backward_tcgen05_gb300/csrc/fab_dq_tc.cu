@@ -411,9 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < 3; ++k)
         for (int i = 0; i < p.pad_n[k]; ++i) p.pad[k][i] = 0.f;
-    // A unit's first global reads (this thread's LSE, its half row of O for
-    // D_i, its first mask chunk) are issued before the previous unit's
-    // epilogue, so their latency hides behind it.
+    // A unit's first global reads (this thread's LSE, half of its share of
+    // O for D_i, its first mask chunk) are issued before the previous unit's
+    // epilogue, so their latency hides behind it; the other half of O is
+    // read at the unit's start (all of it would not stay in registers).
     constexpr int CPH = D / 16;      // 16-byte chunks per half row
     constexpr int RPI = 32 / CPH;    // rows per load instruction
     uint4 ov[CPH];
@@ -432,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // l % CPH of (this warp's) row i * RPI + l / CPH, so a row is full
         // cache lines rather than one sector per thread
 #pragma unroll
-        for (int i = 0; i < CPH; ++i) {
+        for (int i = 0; i < CPH / 2; ++i) {
           const int64_t nr = (int64_t)y.n0 + (warp & 3) * 32 + i * RPI + lane / CPH;
           const int64_t nc = nr < p.N ? nr : p.N - 1;
           ov[i] = ld_global_nc_v4(reinterpret_cast<const uint4*>(p.o + ((y.b * p.N + nc) * p.H + y.h) * D +
@@ -454,6 +455,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // D_i = dO_i . O_i: this thread takes columns hf * D/2 .. hf * D/2 + D/2 - 1
         // of its row (O fetched above, dO from the swizzled tile in shared
         // memory); the two halves meet in shared memory
+#pragma unroll
+        for (int i = CPH / 2; i < CPH; ++i) {
+          const int64_t nr = (int64_t)x.n0 + (warp & 3) * 32 + i * RPI + lane / CPH;
+          const int64_t nc = nr < p.N ? nr : p.N - 1;
+          ov[i] = ld_global_nc_v4(reinterpret_cast<const uint4*>(p.o + ((x.b * p.N + nc) * p.H + x.h) * D +
+                                                                 hf * (D / 2) + (lane % CPH) * 8));
+        }
         const bool got = __all_sync(0xffffffffu, mbar_wait(bar(Q_QF), k & 1, abort_flag, err));
         float part = 0.f;
         if (got) {

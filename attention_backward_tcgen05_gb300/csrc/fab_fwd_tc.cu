@@ -301,8 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax
     // warps 2-5 take keys 0-63 of a tile, warps 6-9 keys 64-127; thread =
     // query row.  The two halves of a row trade their maxima through shared
-    // memory once per tile (an OR-reducing named barrier, so an error ends
-    // every softmax thread's loop at the same tile).
+    // memory once per tile: warps w and w + 4 (the same rows) meet at named
+    // barrier 1 + w % 4, OR-reducing an error flag so both leave their loop
+    // at the same tile; the other pairs run on.
     const int hf = (warp - 2) >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 64; ++e) hmax = fmaxf(hmax, sv[e]);
         }
         mx[((g & 1) * 2 + hf) * C::BQ + r] = hmax;
-        if (named_bar_or(1, kSoftmaxThreads, !(got && ok))) {
+        if (named_bar_or(1 + (warp & 3), 64, !(got && ok))) {
           ok = false;
           break;
         }
@@ -438,16 +439,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // lets both halves finish reading the maxima there, the second
       // publishes l.  Then O has been read: the next unit's first PV may
       // overwrite it.  (A warp whose wait failed reaches the first barrier
-      // too, so every softmax thread leaves together.)
+      // too, so both warps of the pair leave together.)
       const int G = g - 1;  // the unit's last tile
       const bool done =
           ok && __all_sync(0xffffffffu, mbar_wait(bar(F_PV + G % 3), (G / 3) & 1, abort_flag, err));
-      if (named_bar_or(1, kSoftmaxThreads, !done || *abort_flag != 0u)) {
+      if (named_bar_or(1 + (warp & 3), 64, !done || *abort_flag != 0u)) {
         ok = false;
         break;
       }
       mx[((G & 1) * 2 + hf) * C::BQ + r] = l;
-      named_bar_sync(1, kSoftmaxThreads);
+      named_bar_sync(1 + (warp & 3), 64);
       tc_fence_after();
       const float lt = l + mx[((G & 1) * 2 + (hf ^ 1)) * C::BQ + r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
