@@ -454,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (FUSE_D) {
         // D_i = dO_i . O_i: this thread takes columns hf * D/2 .. hf * D/2 + D/2 - 1
         // of its row (O fetched above, dO from the swizzled tile in shared
-        // memory); the two halves meet in shared memory
+        // memory); the two halves meet in shared memory, the two warps of
+        // the rows (w and w + 4) at named barrier 1 + w % 4
 #pragma unroll
         for (int i = CPH / 2; i < CPH; ++i) {
           const int64_t nr = (int64_t)x.n0 + (warp & 3) * 32 + i * RPI + lane / CPH;
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         dpart[hf * C::BQ + r] = row_ok ? part : 0.f;
-        named_bar_sync(2, kSoftmaxThreads);
+        named_bar_sync(1 + (warp & 3), 64);
         di = dpart[r] + dpart[C::BQ + r];
         if (hf == 0 && row_ok) p.di[rowidx] = di;
       } else {
@@ -653,8 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(Q_DF));
       mbar_arrive(bar(Q_STG));
-      // every softmax thread takes the same branch below
-      if (named_bar_or(1, kSoftmaxThreads, !write || *abort_flag != 0u)) break;
+      // both warps of the rows (w and w + 4, named barrier 5 + w % 4) take
+      // the same branch below, so the D_i barrier of the next unit pairs up
+      if (named_bar_or(5 + (warp & 3), 64, !write || *abort_flag != 0u)) break;
     }
   }
 
