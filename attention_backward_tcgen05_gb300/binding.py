@@ -23,7 +23,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfab.so")
 
 FAB_OK, FAB_ERR_INVALID, FAB_ERR_UNSUPPORTED, FAB_ERR_WORKSPACE, FAB_ERR_CUDA, FAB_ERR_TIMEOUT = range(6)
-FAB_F32, FAB_BF16 = 0, 1
+FAB_F32, FAB_BF16, FAB_F16 = 0, 1, 2
 
 EXPORTS = ("fab_version", "fab_status_string", "fab_packed_offsets", "fab_packed_bytes",
            "fab_backward_workspace_bytes", "fab_backward_recompute_workspace_bytes", "fab_forward_lse",
@@ -115,7 +115,9 @@ def dtype_code(t: torch.Tensor) -> int:
         return FAB_F32
     if t.dtype == torch.bfloat16:
         return FAB_BF16
-    raise ValueError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+    if t.dtype == torch.float16:
+        return FAB_F16
+    raise ValueError(f"unsupported dtype {t.dtype}: float32, bfloat16 or float16")
 
 
 def _stream(stream) -> ctypes.c_void_p:

@@ -74,7 +74,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
 
-template <int D>
+template <int D, bool F16 = false>
 struct Cfg {
   static constexpr int BM = 128;  // keys per CTA (tensor-memory lanes)
   static constexpr int BQ = 128;  // queries per step
@@ -98,8 +98,8 @@ struct Cfg {
   // tensor-memory columns: tile buffer b at 128 b (b = 0, 1)
   static constexpr uint32_t TM_X = 128, TM_DV = 256, TM_DK = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
-  static constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);
-  static constexpr uint32_t ID_DVK = idesc_bf16(128, D, false, true);
+  static constexpr uint32_t ID_S = idesc_16(128, BQ, false, false, F16);
+  static constexpr uint32_t ID_DVK = idesc_16(128, D, false, true, F16);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_DK + D <= TM_COLS, "tensor memory budget");
   // epilogue staging (f32, 32-column atoms): dV over the key and value
@@ -140,13 +140,13 @@ struct Params {
   float* dv;
 };
 
-template <int D, bool MASK>
+template <int D, bool MASK, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                   const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   if (smem_u32(smem_raw) & 1023u) {  // swizzled tiles need a 1024-byte-aligned base
@@ -631,8 +631,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; e += 2) {
               const int jj = q4 * 4 + e;  // column within the half
               const float p0 = pv[hh * 32 + jj], p1 = pv[hh * 32 + jj + 1];
-              pk[jj >> 1] = pack_bf16x2(p0, p1);
-              pk[16 + (jj >> 1)] = pack_bf16x2(p0 * (__uint_as_float(ra[jj]) - dv[e]),
+              pk[jj >> 1] = pack2<F16>(p0, p1);
+              pk[16 + (jj >> 1)] = pack2<F16>(p0 * (__uint_as_float(ra[jj]) - dv[e]),
                                                p1 * (__uint_as_float(ra[jj + 1]) - dv[e + 1]));
             }
           }
@@ -701,48 +701,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box, bool f32 = false) {
+              const cuuint32_t* box, CUtensorMapDataType dt) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+  CUresult r = enc(map, dt, (cuuint32_t)rank,
                    const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool MASK>
+template <int D, bool MASK, bool F16>
 cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F16>;
+  const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap mq, mk, mv, mo, mdk, mdv;
   const cuuint64_t e = 2;  // bytes per bf16
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
     const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.N * D * e};
     const cuuint32_t box[3] = {64, (cuuint32_t)C::BQ, 1};
-    if (!make_map(&mq, pr.q, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mq, pr.q, 3, dims, str, box, dt)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.M, (cuuint64_t)(pr.Hkv * pr.B)};
     const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.M * D * e};
     const cuuint32_t box[3] = {64, (cuuint32_t)C::BM, 1};
-    if (!make_map(&mk, pr.k, 3, dims, str, box)) return cudaErrorInvalidValue;
-    if (!make_map(&mv, pr.v, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mk, pr.k, 3, dims, str, box, dt)) return cudaErrorInvalidValue;
+    if (!make_map(&mv, pr.v, 3, dims, str, box, dt)) return cudaErrorInvalidValue;
   }
   {
     // d [DV,H,N,B]: rows n of one head are H*DV elements apart
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)pr.H, (cuuint64_t)pr.N, (cuuint64_t)pr.B};
     const cuuint64_t str[3] = {D * e, (cuuint64_t)pr.H * D * e, (cuuint64_t)pr.N * pr.H * D * e};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)C::BQ, 1};
-    if (!make_map(&mo, pr.d, 4, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mo, pr.d, 4, dims, str, box, dt)) return cudaErrorInvalidValue;
   }
   {
     // the packed f32 dK and dV slices [D,M,Hkv,B], stored in 32-column (128-byte) boxes
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.M, (cuuint64_t)(pr.Hkv * pr.B)};
     const cuuint64_t str[2] = {D * 4, (cuuint64_t)pr.M * D * 4};
     const cuuint32_t box[3] = {32, (cuuint32_t)C::BM, 1};
-    if (!make_map(&mdk, pr.packed + pr.off_k / 4, 3, dims, str, box, true)) return cudaErrorInvalidValue;
-    if (!make_map(&mdv, pr.packed + pr.off_v / 4, 3, dims, str, box, true)) return cudaErrorInvalidValue;
+    const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    if (!make_map(&mdk, pr.packed + pr.off_k / 4, 3, dims, str, box, f32)) return cudaErrorInvalidValue;
+    if (!make_map(&mdv, pr.packed + pr.off_v / 4, 3, dims, str, box, f32)) return cudaErrorInvalidValue;
   }
   Params p;
   p.B = pr.B;
@@ -764,16 +766,16 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const int64_t grid = units < sms ? units : sms;
   cudaError_t err =
-      cudaFuncSetAttribute(bwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      cudaFuncSetAttribute(bwd_tc_kernel<D, MASK, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  bwd_tc_kernel<D, MASK><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdk, mdv, p);
+  bwd_tc_kernel<D, MASK, F16><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdk, mdv, p);
   return cudaPeekAtLastError();
 }
 
 }  // namespace
 
 bool backward_tc_supported(const Problem& p) {
-  if (p.dtype != FAB_BF16 || p.DK != p.DV) return false;
+  if ((p.dtype != FAB_BF16 && p.dtype != FAB_F16) || p.DK != p.DV) return false;
   if (p.DK != 64 && p.DK != 128) return false;
   // TMA coordinates are 32-bit; grid.x must fit as well
   if (p.N >= (1ll << 31) || p.M >= (1ll << 31) || p.H * p.B >= (1ll << 31)) return false;
@@ -784,8 +786,12 @@ bool backward_tc_supported(const Problem& p) {
 
 cudaError_t launch_backward_tc(const Problem& p, cudaStream_t s) {
   const bool m = p.mask != nullptr;
-  if (p.DK == 128) return m ? launch_d<128, true>(p, s) : launch_d<128, false>(p, s);
-  return m ? launch_d<64, true>(p, s) : launch_d<64, false>(p, s);
+  if (p.dtype == FAB_F16) {
+    if (p.DK == 128) return m ? launch_d<128, true, true>(p, s) : launch_d<128, false, true>(p, s);
+    return m ? launch_d<64, true, true>(p, s) : launch_d<64, false, true>(p, s);
+  }
+  if (p.DK == 128) return m ? launch_d<128, true, false>(p, s) : launch_d<128, false, false>(p, s);
+  return m ? launch_d<64, true, false>(p, s) : launch_d<64, false, false>(p, s);
 }
 
 uint32_t take_error_tc() {

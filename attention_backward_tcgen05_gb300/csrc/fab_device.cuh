@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -260,6 +261,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same for A and B both f16 (f16 = true: A and B format 0) or both bf16.
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool a_mn_major, bool b_mn_major, bool f16) {
+  return f16 ? idesc_bf16(M, N, a_mn_major, b_mn_major) & ~((7u << 7) | (7u << 10))
+             : idesc_bf16(M, N, a_mn_major, b_mn_major);
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand:
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4,
 //   32-45 stride byte offset >> 4, 46-47 version (1), 61-63 layout (2 = SW128).
@@ -347,6 +354,26 @@ FAB_DEV float ex2_approx(float x) {
 FAB_DEV uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits), .y = hi
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two values of the 16-bit input type (f16 when F16, else bf16), packed as
+// the tensor core reads them (lo in the low 16 bits), and back.
+template <bool F16>
+FAB_DEV uint32_t pack2(float lo, float hi) {
+  if constexpr (F16) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    return pack_bf16x2(lo, hi);
+  }
+}
+template <bool F16>
+FAB_DEV float2 unpack2(uint32_t v) {
+  if constexpr (F16) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+  } else {
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+  }
 }
 
 FAB_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {

@@ -57,7 +57,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
 
-template <int D>
+template <int D, bool F16 = false>
 struct QCfg {
   static constexpr int BQ = 128;  // queries per CTA (tensor-memory lanes)
   static constexpr int BK = 128;  // keys per tile
@@ -81,8 +81,8 @@ struct QCfg {
   static constexpr uint32_t TM_BUF = 128;  // buffer b at columns 128 b, b = 0, 1, 2
   static constexpr uint32_t TM_DQ = 384;
   static constexpr uint32_t TM_COLS = 512;
-  static constexpr uint32_t ID_S = idesc_bf16(128, BK, false, false);
-  static constexpr uint32_t ID_DQ = idesc_bf16(128, D, false, true);
+  static constexpr uint32_t ID_S = idesc_16(128, BK, false, false, F16);
+  static constexpr uint32_t ID_DQ = idesc_16(128, D, false, true, F16);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_DQ + D <= TM_COLS, "tensor memory budget");
   static_assert(D * 128 * 4 == 2 * TILE, "dQ staging: one key stage per half of the columns");
@@ -117,17 +117,17 @@ struct QParams {
   float* di;  // read, or written with FUSE_D
   const uint16_t* mask;
   float* dq;
-  const __nv_bfloat16* o;  // forward output [D,H,N,B], read with FUSE_D
+  const uint16_t* o;  // forward output [D,H,N,B] (16-bit input type), read with FUSE_D
   float* pad[3];           // the packed result's padding after each slice, zeroed with FUSE_D
   int pad_n[3];
 };
 
-template <int D, bool FUSE_D>
+template <int D, bool FUSE_D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                  const __grid_constant__ CUtensorMap tmDQ, const QParams p) {
-  using C = QCfg<D>;
+  using C = QCfg<D, F16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -467,8 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float part = 0.f;
         if (got) {
           auto dot2 = [](uint32_t a, uint32_t b) {
-            return __uint_as_float(a << 16) * __uint_as_float(b << 16) +
-                   __uint_as_float(a & 0xffff0000u) * __uint_as_float(b & 0xffff0000u);
+            const float2 fa = unpack2<F16>(a), fb = unpack2<F16>(b);
+            return fa.x * fb.x + fa.y * fb.y;
           };
           // chunk l % CPH of row i * RPI + l / CPH (as loaded), against the
           // same chunk of dO from the swizzled tile; the CPH lanes of a row
@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int e = 2 * c;
           const float d0 = __uint_as_float(e < 32 ? ra[e] : rb[e - 32]);
           const float d1 = __uint_as_float(e + 1 < 32 ? ra[e + 1] : rb[e + 1 - 32]);
-          pk[c] = pack_bf16x2(pv[e] * (d0 - di), pv[e + 1] * (d1 - di));
+          pk[c] = pack2<F16>(pv[e] * (d0 - di), pv[e + 1] * (d1 - di));
         }
         // packed dS over the first 32 of this warp's own 64 dP columns (the
         // other warp of the lane quarter reads only its own columns)
@@ -669,47 +669,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box, bool f32 = false) {
+              const cuuint32_t* box, CUtensorMapDataType dt) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+  return enc(map, dt, (cuuint32_t)rank,
              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool FUSE_D>
+template <int D, bool FUSE_D, bool F16>
 cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
-  using C = QCfg<D>;
+  using C = QCfg<D, F16>;
+  const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap mq, mk, mv, mo, mdq;
   const cuuint64_t e = 2;  // bytes per bf16
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
     const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.N * D * e};
     const cuuint32_t box[3] = {64, (cuuint32_t)C::BQ, 1};
-    if (!make_map(&mq, pr.q, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mq, pr.q, 3, dims, str, box, dt)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.M, (cuuint64_t)(pr.Hkv * pr.B)};
     const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.M * D * e};
     const cuuint32_t box[3] = {64, (cuuint32_t)C::BK, 1};
-    if (!make_map(&mk, pr.k, 3, dims, str, box)) return cudaErrorInvalidValue;
-    if (!make_map(&mv, pr.v, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mk, pr.k, 3, dims, str, box, dt)) return cudaErrorInvalidValue;
+    if (!make_map(&mv, pr.v, 3, dims, str, box, dt)) return cudaErrorInvalidValue;
   }
   {
     // d [DV,H,N,B]: rows n of one head are H*DV elements apart
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)pr.H, (cuuint64_t)pr.N, (cuuint64_t)pr.B};
     const cuuint64_t str[3] = {D * e, (cuuint64_t)pr.H * D * e, (cuuint64_t)pr.N * pr.H * D * e};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)C::BQ, 1};
-    if (!make_map(&mo, pr.d, 4, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mo, pr.d, 4, dims, str, box, dt)) return cudaErrorInvalidValue;
   }
   {
     // the packed f32 dQ slice [D,N,H,B], stored in 32-column (128-byte) boxes
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
     const cuuint64_t str[2] = {D * 4, (cuuint64_t)pr.N * D * 4};
     const cuuint32_t box[3] = {32, (cuuint32_t)C::BQ, 1};
-    if (!make_map(&mdq, pr.packed, 3, dims, str, box, true)) return cudaErrorInvalidValue;
+    if (!make_map(&mdq, pr.packed, 3, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return cudaErrorInvalidValue;
   }
   QParams p;
   p.B = pr.B;
@@ -723,7 +724,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   p.di = pr.di;
   p.mask = pr.mask;
   p.dq = pr.packed;
-  p.o = static_cast<const __nv_bfloat16*>(pr.o);
+  p.o = static_cast<const uint16_t*>(pr.o);
   {
     const int64_t nq = D * pr.N * pr.H * pr.B, nk = D * pr.M * pr.Hkv * pr.B;
     p.pad[0] = pr.packed + nq;
@@ -740,17 +741,21 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const int64_t grid = units < sms ? units : sms;
   cudaError_t err =
-      cudaFuncSetAttribute(dq_tc_kernel<D, FUSE_D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      cudaFuncSetAttribute(dq_tc_kernel<D, FUSE_D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  dq_tc_kernel<D, FUSE_D><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdq, p);
+  dq_tc_kernel<D, FUSE_D, F16><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdq, p);
   return cudaPeekAtLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_dq_tc(const Problem& p, bool fuse_d, cudaStream_t s) {
-  if (fuse_d) return p.DK == 128 ? launch_d<128, true>(p, s) : launch_d<64, true>(p, s);
-  return p.DK == 128 ? launch_d<128, false>(p, s) : launch_d<64, false>(p, s);
+  if (p.dtype == FAB_F16) {
+    if (fuse_d) return p.DK == 128 ? launch_d<128, true, true>(p, s) : launch_d<64, true, true>(p, s);
+    return p.DK == 128 ? launch_d<128, false, true>(p, s) : launch_d<64, false, true>(p, s);
+  }
+  if (fuse_d) return p.DK == 128 ? launch_d<128, true, false>(p, s) : launch_d<64, true, false>(p, s);
+  return p.DK == 128 ? launch_d<128, false, false>(p, s) : launch_d<64, false, false>(p, s);
 }
 
 uint32_t take_error_dq() {

@@ -44,7 +44,7 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
 
-template <int D>
+template <int D, bool F16 = false>
 struct FCfg {
   static constexpr int BQ = 128;  // queries per CTA (tensor-memory lanes)
   static constexpr int BK = 128;  // keys per tile
@@ -65,8 +65,8 @@ struct FCfg {
   static constexpr uint32_t TM_S = 0;  // + 128 * buffer, buffers 0..2
   static constexpr uint32_t TM_O = 384;
   static constexpr uint32_t TM_COLS = 512;
-  static constexpr uint32_t ID_S = idesc_bf16(128, BK, false, false);
-  static constexpr uint32_t ID_PV = idesc_bf16(128, D, false, true);
+  static constexpr uint32_t ID_S = idesc_16(128, BK, false, false, F16);
+  static constexpr uint32_t ID_PV = idesc_16(128, D, false, true, F16);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
 };
@@ -90,16 +90,16 @@ struct FParams {
   float scale;
   int causal;
   const uint16_t* mask;
-  __nv_bfloat16* o;
+  void* o;
   float* lse;
 };
 
-template <int D, bool MASK>
+template <int D, bool MASK, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmOut,
                   const FParams p) {
-  using C = FCfg<D>;
+  using C = FCfg<D, F16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   if (smem_u32(smem_raw) & 1023u) {  // swizzled tiles need a 1024-byte-aligned base
@@ -423,9 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const uint32_t packed = pack_bf16x2(ex2_approx(sv[2 * c] - m_use), ex2_approx(sv[2 * c + 1] - m_use));
-          // sum what the tensor core will see (the bf16-rounded P)
-          rsum += __uint_as_float(packed << 16) + __uint_as_float(packed & 0xffff0000u);
+          const uint32_t packed = pack2<F16>(ex2_approx(sv[2 * c] - m_use), ex2_approx(sv[2 * c + 1] - m_use));
+          // sum what the tensor core will see (P rounded to the input type)
+          const float2 pr = unpack2<F16>(packed);
+          rsum += pr.x + pr.y;
           pk[c] = packed;
         }
         tmem_st32(tS + hf * 32, pk);
@@ -467,10 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; e += 8) {
           const int ch = ((col + e) % 64) / 8;  // 16-byte chunk within the 128-byte row
           st_shared_v4(st + (uint32_t)((col + e) / 64) * C::ATOM + r * 128 + ((ch ^ (r & 7)) << 4),
-                       pack_bf16x2(__uint_as_float(ra[e]) * inv, __uint_as_float(ra[e + 1]) * inv),
-                       pack_bf16x2(__uint_as_float(ra[e + 2]) * inv, __uint_as_float(ra[e + 3]) * inv),
-                       pack_bf16x2(__uint_as_float(ra[e + 4]) * inv, __uint_as_float(ra[e + 5]) * inv),
-                       pack_bf16x2(__uint_as_float(ra[e + 6]) * inv, __uint_as_float(ra[e + 7]) * inv));
+                       pack2<F16>(__uint_as_float(ra[e]) * inv, __uint_as_float(ra[e + 1]) * inv),
+                       pack2<F16>(__uint_as_float(ra[e + 2]) * inv, __uint_as_float(ra[e + 3]) * inv),
+                       pack2<F16>(__uint_as_float(ra[e + 4]) * inv, __uint_as_float(ra[e + 5]) * inv),
+                       pack2<F16>(__uint_as_float(ra[e + 6]) * inv, __uint_as_float(ra[e + 7]) * inv));
         }
       }
       fence_proxy_async_smem();
@@ -491,42 +492,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 bool make_map(CUtensorMap* map, const void* base, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box) {
+              const cuuint32_t* box, CUtensorMapDataType dt) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   cuuint32_t es[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+  return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_map4(CUtensorMap* map, const void* base, const cuuint64_t* dims, const cuuint64_t* strides,
-               const cuuint32_t* box) {
+               const cuuint32_t* box, CUtensorMapDataType dt) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+  return enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool MASK>
+template <int D, bool MASK, bool F16>
 cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
-  using C = FCfg<D>;
+  using C = FCfg<D, F16>;
+  const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap mq, mk, mv, mo;
   const cuuint64_t e = 2;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
     const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.N * D * e};
     const cuuint32_t box[3] = {64, (cuuint32_t)C::BQ, 1};
-    if (!make_map(&mq, pr.q, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mq, pr.q, dims, str, box, dt)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.M, (cuuint64_t)(pr.Hkv * pr.B)};
     const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.M * D * e};
     const cuuint32_t box[3] = {64, (cuuint32_t)C::BK, 1};
-    if (!make_map(&mk, pr.k, dims, str, box)) return cudaErrorInvalidValue;
-    if (!make_map(&mv, pr.v, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mk, pr.k, dims, str, box, dt)) return cudaErrorInvalidValue;
+    if (!make_map(&mv, pr.v, dims, str, box, dt)) return cudaErrorInvalidValue;
   }
   {
     // O [DV,H,N,B]: rows n of one head are H*DV elements apart; stored in
@@ -534,7 +536,7 @@ cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)pr.H, (cuuint64_t)pr.N, (cuuint64_t)pr.B};
     const cuuint64_t str[3] = {D * e, (cuuint64_t)pr.H * D * e, (cuuint64_t)pr.N * pr.H * D * e};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)C::BQ, 1};
-    if (!make_map4(&mo, o, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map4(&mo, o, dims, str, box, dt)) return cudaErrorInvalidValue;
   }
   FParams p;
   p.B = pr.B;
@@ -545,7 +547,7 @@ cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
   p.scale = pr.scale;
   p.causal = pr.causal;
   p.mask = pr.mask;
-  p.o = static_cast<__nv_bfloat16*>(o);
+  p.o = o;
   p.lse = lse;
   // persistent: one CTA per SM (each owns the SM's tensor memory), walking units
   const int64_t units = ((pr.N + C::BQ - 1) / C::BQ) * pr.H * pr.B;
@@ -554,16 +556,16 @@ cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const int64_t grid = units < sms ? units : sms;
   cudaError_t err =
-      cudaFuncSetAttribute(fwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      cudaFuncSetAttribute(fwd_tc_kernel<D, MASK, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  fwd_tc_kernel<D, MASK><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, p);
+  fwd_tc_kernel<D, MASK, F16><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, p);
   return cudaPeekAtLastError();
 }
 
 }  // namespace
 
 bool forward_tc_supported(const Problem& p) {
-  if (p.dtype != FAB_BF16 || p.DK != p.DV) return false;
+  if ((p.dtype != FAB_BF16 && p.dtype != FAB_F16) || p.DK != p.DV) return false;
   if (p.DK != 64 && p.DK != 128) return false;
   if (p.N >= (1ll << 31) || p.M >= (1ll << 31) || p.H * p.B >= (1ll << 31)) return false;
   if (((p.N + 127) / 128) * p.H * p.B >= (1ll << 31)) return false;
@@ -572,8 +574,12 @@ bool forward_tc_supported(const Problem& p) {
 
 cudaError_t launch_forward_tc(const Problem& p, void* o, float* lse, cudaStream_t s) {
   const bool m = p.mask != nullptr;
-  if (p.DK == 128) return m ? launch_d<128, true>(p, o, lse, s) : launch_d<128, false>(p, o, lse, s);
-  return m ? launch_d<64, true>(p, o, lse, s) : launch_d<64, false>(p, o, lse, s);
+  if (p.dtype == FAB_F16) {
+    if (p.DK == 128) return m ? launch_d<128, true, true>(p, o, lse, s) : launch_d<128, false, true>(p, o, lse, s);
+    return m ? launch_d<64, true, true>(p, o, lse, s) : launch_d<64, false, true>(p, o, lse, s);
+  }
+  if (p.DK == 128) return m ? launch_d<128, true, false>(p, o, lse, s) : launch_d<128, false, false>(p, o, lse, s);
+  return m ? launch_d<64, true, false>(p, o, lse, s) : launch_d<64, false, false>(p, o, lse, s);
 }
 
 uint32_t take_error_fwd() {

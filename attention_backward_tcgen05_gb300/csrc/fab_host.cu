@@ -70,7 +70,7 @@ size_t di_bytes(const fab_dims* d) {
 // The forward output O [DV,H,N,B] and the row LSE [N,H,B] that fab_backward
 // keeps in its workspace, after D_i, when the caller passes neither.
 size_t o_bytes(const fab_dims* d, int dtype) {
-  const size_t b = (size_t)(d->B * d->H * d->N * d->DV) * (dtype == FAB_BF16 ? 2u : 4u);
+  const size_t b = (size_t)(d->B * d->H * d->N * d->DV) * (dtype == FAB_F32 ? 4u : 2u);
   return (b + 255) / 256 * 256;
 }
 size_t recompute_bytes(const fab_dims* d, int dtype) { return di_bytes(d) + o_bytes(d, dtype) + di_bytes(d); }
@@ -91,7 +91,7 @@ Problem make_problem(const fab_dims* d, int dtype, float scale, int causal) {
   return p;
 }
 
-bool dtype_ok(int dtype) { return dtype == FAB_F32 || dtype == FAB_BF16; }
+bool dtype_ok(int dtype) { return dtype == FAB_F32 || dtype == FAB_BF16 || dtype == FAB_F16; }
 
 bool widths_supported(const fab_dims* d) { return d->DK <= kMaxWidth && d->DV <= kMaxWidth; }
 

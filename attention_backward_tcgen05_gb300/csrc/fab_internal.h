@@ -18,7 +18,7 @@ struct Problem {
   int64_t B, H, Hkv, N, M, DK, DV;
   float scale;
   int causal;
-  int dtype;  // FAB_F32 or FAB_BF16
+  int dtype;  // FAB_F32, FAB_BF16 or FAB_F16
   const void* q;
   const void* k;
   const void* v;

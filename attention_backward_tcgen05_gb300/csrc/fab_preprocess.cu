@@ -6,6 +6,7 @@
 //   plus the zero fill of the packed result's padding (ggmlR packing test: the
 //   whole buffer is zeroed and padding stays 0).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "fab.h"
 #include "fab_device.cuh"
@@ -37,8 +38,22 @@ struct Vec<__nv_bfloat16> {
   }
 };
 
+template <>
+struct Vec<__half> {
+  static constexpr int kElems = 8;
+  static __device__ __forceinline__ float dot2(uint32_t a, uint32_t b) {
+    const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&a));
+    const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&b));
+    return fa.x * fb.x + fa.y * fb.y;
+  }
+  static __device__ __forceinline__ float dot(const uint4& a, const uint4& b) {
+    return dot2(a.x, b.x) + dot2(a.y, b.y) + dot2(a.z, b.z) + dot2(a.w, b.w);
+  }
+};
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 
 struct ZeroRange {
   float* ptr;
@@ -129,7 +144,7 @@ cudaError_t launch_preprocess(const Problem& p, cudaStream_t s) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // lanes per row: enough 16-byte chunks for every lane, at most a warp
-  const int elems = p.dtype == FAB_BF16 ? 8 : 4;
+  const int elems = p.dtype == FAB_F32 ? 4 : 8;
   int lpr = 32;
   if (p.DV % elems == 0) {
     const int64_t chunks = p.DV / elems;
@@ -144,6 +159,10 @@ cudaError_t launch_preprocess(const Problem& p, cudaStream_t s) {
     preprocess_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(p.d), static_cast<const __nv_bfloat16*>(p.o), p.di, rows, (int)p.DV, p.H,
         p.N, lpr, pa, pb, pc);
+  } else if (p.dtype == FAB_F16) {
+    preprocess_kernel<__half><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const __half*>(p.d),
+                                                               static_cast<const __half*>(p.o), p.di, rows, (int)p.DV,
+                                                               p.H, p.N, lpr, pa, pb, pc);
   } else {
     preprocess_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const float*>(p.d),
                                                               static_cast<const float*>(p.o), p.di, rows, (int)p.DV,

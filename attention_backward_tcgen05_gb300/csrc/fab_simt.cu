@@ -28,8 +28,10 @@ constexpr int kWarps = 8;  // warps per block
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 __device__ __forceinline__ void from_f32(float& dst, float x) { dst = x; }
 __device__ __forceinline__ void from_f32(__nv_bfloat16& dst, float x) { dst = __float2bfloat16_rn(x); }
+__device__ __forceinline__ void from_f32(__half& dst, float x) { dst = __float2half_rn(x); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -241,24 +243,36 @@ int regs_per_lane(const Problem& p) {
   return (int)((w + 31) / 32);
 }
 
+// widths up to 32 R per lane
+template <typename T>
+cudaError_t fwd_t(const Problem& p, int r, void* o, float* lse, cudaStream_t s) {
+  if (r <= 1) return fwd_r<T, 1>(p, o, lse, s);
+  if (r <= 2) return fwd_r<T, 2>(p, o, lse, s);
+  if (r <= 4) return fwd_r<T, 4>(p, o, lse, s);
+  return fwd_r<T, 8>(p, o, lse, s);
+}
+template <typename T>
+cudaError_t bwd_t(const Problem& p, int r, cudaStream_t s) {
+  if (r <= 1) return bwd_r<T, 1>(p, s);
+  if (r <= 2) return bwd_r<T, 2>(p, s);
+  if (r <= 4) return bwd_r<T, 4>(p, s);
+  return bwd_r<T, 8>(p, s);
+}
+
 }  // namespace
 
 cudaError_t launch_forward_simt(const Problem& p, void* o, float* lse, cudaStream_t s) {
   const int r = regs_per_lane(p);
-  const bool bf = p.dtype == FAB_BF16;
-  if (r <= 1) return bf ? fwd_r<__nv_bfloat16, 1>(p, o, lse, s) : fwd_r<float, 1>(p, o, lse, s);
-  if (r <= 2) return bf ? fwd_r<__nv_bfloat16, 2>(p, o, lse, s) : fwd_r<float, 2>(p, o, lse, s);
-  if (r <= 4) return bf ? fwd_r<__nv_bfloat16, 4>(p, o, lse, s) : fwd_r<float, 4>(p, o, lse, s);
-  return bf ? fwd_r<__nv_bfloat16, 8>(p, o, lse, s) : fwd_r<float, 8>(p, o, lse, s);
+  if (p.dtype == FAB_BF16) return fwd_t<__nv_bfloat16>(p, r, o, lse, s);
+  if (p.dtype == FAB_F16) return fwd_t<__half>(p, r, o, lse, s);
+  return fwd_t<float>(p, r, o, lse, s);
 }
 
 cudaError_t launch_backward_simt(const Problem& p, cudaStream_t s) {
   const int r = regs_per_lane(p);
-  const bool bf = p.dtype == FAB_BF16;
-  if (r <= 1) return bf ? bwd_r<__nv_bfloat16, 1>(p, s) : bwd_r<float, 1>(p, s);
-  if (r <= 2) return bf ? bwd_r<__nv_bfloat16, 2>(p, s) : bwd_r<float, 2>(p, s);
-  if (r <= 4) return bf ? bwd_r<__nv_bfloat16, 4>(p, s) : bwd_r<float, 4>(p, s);
-  return bf ? bwd_r<__nv_bfloat16, 8>(p, s) : bwd_r<float, 8>(p, s);
+  if (p.dtype == FAB_BF16) return bwd_t<__nv_bfloat16>(p, r, s);
+  if (p.dtype == FAB_F16) return bwd_t<__half>(p, r, s);
+  return bwd_t<float>(p, r, s);
 }
 
 }  // namespace fab

@@ -30,7 +30,7 @@ class Workload:
     M: int
     DK: int
     DV: int
-    dtype: str            # "f32" or "bf16": the type q, k, v and d are handed over in
+    dtype: str            # "f32", "bf16" or "f16": the type q, k, v and d are handed over in
     dist: str             # "uniform" (lo, hi) or "normal" (std)
     scale: float
     causal: bool = False
@@ -80,7 +80,9 @@ def _draw(g, shape, w: Workload):
         x = torch.randn(shape, generator=g, dtype=torch.float32) * w.std
     else:
         raise ValueError(w.dist)
-    return x.to(torch.bfloat16) if w.dtype == "bf16" else x
+    if w.dtype == "bf16":
+        return x.to(torch.bfloat16)
+    return x.to(torch.float16) if w.dtype == "f16" else x
 
 
 def make(w: Workload, device="cpu"):

@@ -43,8 +43,9 @@
  * CUDA runtime's).  Device-side waits are bounded: a wait that runs out sets
  * an error word that fab_last_device_error() returns as FAB_ERR_TIMEOUT.
  *
- * Supported on the GPU: dtype FAB_F32 (any DK, DV <= 256) and FAB_BF16
- * (tensor-core path when DK == DV and DK is 64 or 128; any DK, DV <= 256
+ * Supported on the GPU: dtype FAB_F32 (any DK, DV <= 256), FAB_BF16 and
+ * FAB_F16 (tensor-core path when DK == DV and DK is 64 or 128, with P and dS
+ * rounded to the input type for their products; any DK, DV <= 256
  * otherwise).  Anything else returns FAB_ERR_UNSUPPORTED; there is no CPU
  * fallback.  ALiBi and logit soft-capping are not part of this ABI.
  */
@@ -75,7 +76,8 @@ typedef enum {
 
 typedef enum {
   FAB_F32 = 0,  /* q, k, v, d, o are float32 */
-  FAB_BF16 = 1  /* q, k, v, d, o are bfloat16 */
+  FAB_BF16 = 1, /* q, k, v, d, o are bfloat16 */
+  FAB_F16 = 2   /* q, k, v, d, o are float16 (IEEE binary16) */
 } fab_dtype;
 
 /* Sizes in ggml terms: B batches, H query heads, Hkv key/value heads

@@ -12,7 +12,10 @@ import torch
 import oracle
 from attention_backward_tcgen05_gb300 import binding, inputs
 
-TOL = {"bf16": 1e-2, "f32": 2e-3}
+# max |gpu - oracle| / max |oracle| per slice.  bf16 (unit roundoff 2^-8) and
+# f16 (2^-11) round P and dS to the input type for the tensor core; the f32
+# path computes in f32 throughout.
+TOL = {"bf16": 1e-2, "f16": 5e-3, "f32": 2e-3}
 
 
 def run_gpu(w: inputs.Workload, x: dict):

@@ -81,7 +81,7 @@ def test_recompute_workspace_bytes(L):
     d = binding.make_dims(2, 4, 2, 100, 70, 64, 48)
     r256 = lambda x: (x + 255) // 256 * 256
     rows = 2 * 4 * 100
-    for dt, elem in ((binding.FAB_BF16, 2), (binding.FAB_F32, 4)):
+    for dt, elem in ((binding.FAB_BF16, 2), (binding.FAB_F16, 2), (binding.FAB_F32, 4)):
         want = r256(rows * 4) + r256(rows * 48 * elem) + r256(rows * 4)
         assert binding.fab_backward_recompute_workspace_bytes(d, dt) == want
         assert binding.fab_backward_recompute_workspace_bytes(d, dt) > binding.fab_backward_workspace_bytes(d, dt)
@@ -115,6 +115,7 @@ def test_null_and_misaligned_pointers(L):
         assert call_backward(L, d, {key: FAKE + 4}) == binding.FAB_ERR_INVALID, key
     assert call_backward(L, d, mask=FAKE + 2) == binding.FAB_ERR_INVALID
     assert call_backward(L, d, dtype=5) == binding.FAB_ERR_INVALID
+    assert call_backward(L, d, dtype=3) == binding.FAB_ERR_INVALID
 
 
 def test_workspace_errors(L):

@@ -45,6 +45,11 @@ SMALL = [
     ("simt_f32_mask", 2, 2, 2, 33, 65, 64, 64, "f32", False, "random"),
     ("simt_bf16_odd", 1, 2, 1, 33, 47, 40, 24, "bf16", False, "random"),
     ("simt_f32_wide", 1, 1, 1, 20, 30, 256, 200, "f32", True, "none"),
+    # float16 inputs: the tensor-core passes with f16 operands, the CUDA-core path
+    ("tc128_f16_causal_gqa_mask", 2, 4, 2, 200, 300, 128, 128, "f16", True, "random"),
+    ("tc64_f16_mask_ragged", 1, 4, 2, 96, 130, 64, 64, "f16", False, "random"),
+    ("tc128_f16_many_units", 16, 8, 4, 384, 384, 128, 128, "f16", True, "none"),
+    ("simt_f16_odd", 1, 2, 1, 33, 47, 40, 24, "f16", False, "random"),
     # the pages' packing shape: widths below one 16-byte chunk, DK != DV
     ("simt_f32_dk3_dv5", 2, 4, 2, 37, 29, 3, 5, "f32", False, "random"),
     ("simt_bf16_dk3_dv5", 1, 2, 1, 33, 20, 3, 5, "bf16", True, "none"),
