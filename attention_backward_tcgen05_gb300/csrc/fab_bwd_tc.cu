@@ -1,6 +1,7 @@
 // fab_bwd_tc.cu -- the key/value pass of the attention backward on the
 // fifth-generation tensor cores (tcgen05.mma, accumulators in tensor memory,
-// operands staged by TMA in 128-byte-swizzled shared memory).  bf16 inputs,
+// operands staged by TMA in 128-byte-swizzled shared memory).  bf16 or f16
+// inputs (template parameter F16; P and dS are rounded to the same type),
 // D = DK = DV in {64, 128}, f32 accumulation; writes the dK and dV slices of
 // the packed f32 result.  The query pass (fab_dq_tc.cu) writes dQ.
 //
@@ -33,7 +34,7 @@
 // S^T(i) lands there; the softmax warps read it into registers (P stays in
 // registers), then dP^T(i) lands in the same columns; a warp reads its 64
 // dP^T columns in two halves of 32 queries and writes each half's P^T and
-// dS^T (packed bf16, 16 columns each) over the 32 columns it just read;
+// dS^T (packed 16-bit, 16 columns each) over the 32 columns it just read;
 // dV(i) and dK(i) read them from there.  So dP^T(i) waits only for the
 // softmax warps to read S^T(i), and S^T(i+1) only for dV(i-1), dK(i-1) to
 // finish with the other buffer, while tile i is being worked on.
@@ -82,7 +83,7 @@ struct Cfg {
   static constexpr int OST = D == 128 ? 2 : 4;  // dO ring (with the LSE and D rows)
   static constexpr int ATOMS = D / 64;             // 128-byte swizzle atoms along D
   static constexpr uint32_t ATOM = 128 * 128;      // one 128-row x 128-byte atom column
-  static constexpr uint32_t TILE = ATOMS * ATOM;   // one 128 x D bf16 tile
+  static constexpr uint32_t TILE = ATOMS * ATOM;   // one 128 x D tile of 16-bit elements
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE;
   static constexpr uint32_t OFF_Q = OFF_V + TILE;           // + stage * TILE
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_drain(bar(B_FIN_S), 0);
     } else {
       // dV += P^T dO_g and dK += dS^T Q_g once the softmax warps wrote
-      // P^T(g), dS^T(g) into X: packed bf16, queries 32 c .. 32 c + 31 at
+      // P^T(g), dS^T(g) into X: packed 16-bit, queries 32 c .. 32 c + 31 at
       // columns 32 c + 0..15 (P) and 32 c + 16..31 (dS).  A unit's first
       // products wait for the previous unit's epilogue to have read dV, dK;
       // after its last, this warp writes the staged dV, dK out.
@@ -716,7 +717,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   using C = Cfg<D, F16>;
   const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap mq, mk, mv, mo, mdk, mdv;
-  const cuuint64_t e = 2;  // bytes per bf16
+  const cuuint64_t e = 2;  // bytes per 16-bit element
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
     const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.N * D * e};

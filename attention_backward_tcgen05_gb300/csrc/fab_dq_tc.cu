@@ -1,5 +1,6 @@
 // fab_dq_tc.cu -- the query-gradient pass of the attention backward on the
-// fifth-generation tensor cores.  bf16 inputs, D = DK = DV in {64, 128}, f32
+// fifth-generation tensor cores.  bf16 or f16 inputs (template parameter
+// F16; P and dS are rounded to the same type), D = DK = DV in {64, 128}, f32
 // accumulation; writes the dQ slice of the packed f32 result.
 //
 // Math (labml "Flash Attention", "Backward pass"; ggmlR attn_ref for the mask
@@ -20,7 +21,7 @@
 // Per key tile j (thread = query row, 128 tensor-memory lanes):
 //   S    = Q  K_j^T   [128 x 128]  A = Q (smem, K-major),   B = K_j (K-major)
 //   dP   = dO V_j^T   [128 x 128]  A = dO (smem, K-major),  B = V_j (K-major)
-//   dS   = exp2(S*scale*log2e + mask*log2e - LSE*log2e) * (dP - D) -> bf16,
+//   dS   = exp2(S*scale*log2e + mask*log2e - LSE*log2e) * (dP - D) -> 16-bit,
 //          written over the S columns it came from
 //   dQ  += dS K_j     [128 x D]    A = dS (tmem),           B = K_j (MN-major)
 // Three 128-column tensor-memory buffers rotate: tile j's S lands in buffer
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar(Q_FIN_P), issue);
       mbar_drain(bar(Q_FIN_P), 0);
     } else if (warp == 11) {
-      // dQ += dS(g) K, dS(g) in buffer g + 2 (packed bf16: keys 0-63 at
+      // dQ += dS(g) K, dS(g) in buffer g + 2 (packed 16-bit: keys 0-63 at
       // +0..31, keys 64-127 at +64..95), K MN-major; a unit's first product
       // waits for the previous unit's epilogue to have read dQ
       const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::ATOM, 1024);
@@ -684,7 +685,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   using C = QCfg<D, F16>;
   const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap mq, mk, mv, mo, mdq;
-  const cuuint64_t e = 2;  // bytes per bf16
+  const cuuint64_t e = 2;  // bytes per 16-bit element
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
     const cuuint64_t str[2] = {D * e, (cuuint64_t)pr.N * D * e};

@@ -1,5 +1,6 @@
 // fab_fwd_tc.cu -- attention forward with the row log-sum-exp, on tcgen05.
-// bf16 inputs, D = DK = DV in {64, 128}, f32 accumulation; writes O in bf16
+// bf16 or f16 inputs (template parameter F16), D = DK = DV in {64, 128}, f32
+// accumulation; writes O in the input type
 // ([DV,H,N,B]) and LSE in f32 ([N,H,B], natural log, +inf for a row with no
 // finite score).
 //
@@ -15,7 +16,7 @@
 // ring stages, tensor-memory buffers and barrier phases count tiles across
 // units.  S = Q K_j^T lands in one of three
 // tensor-memory buffers, so the MMAs for the next tiles run while the softmax
-// warps turn tile j into P (bf16, written back over S) and the tensor core
+// warps turn tile j into P (input type, written back over S) and the tensor core
 // then accumulates O += P V_j in tensor memory.  The running max is only
 // raised when a tile's max exceeds it by more than 8 (in log2 units); P is
 // then bounded by 2^8 and O is rescaled in tensor memory only on those rare
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar(F_FIN_S), issue);
       mbar_drain(bar(F_FIN_S), 0);
     } else {
-      // O += P(g) V_g once the softmax warps wrote P(g): packed bf16, key e
+      // O += P(g) V_g once the softmax warps wrote P(g): packed 16-bit, key e
       // at column e / 2 of buffer g % 3; a unit's first product waits for
       // the previous unit's epilogue to have read O.  After a unit's last
       // product, once the softmax warps staged O/l, this warp writes it out
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         m_run = m_new;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        // P = exp2(x - m), packed bf16: key hf * 64 + e at column hf * 32 + e / 2
+        // P = exp2(x - m), packed 16-bit: key hf * 64 + e at column hf * 32 + e / 2
         float rsum = 0.f;
         uint32_t pk[32];
 #pragma unroll
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float lt = l + mx[((G & 1) * 2 + (hf ^ 1)) * C::BQ + r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      // O / l in bf16, staged in the key tile of the last stage as 64-column
+      // O / l in the input type, staged in the key tile of the last stage as 64-column
       // atoms of 128-byte swizzled rows (that stage's products are done; the
       // producer holds K_{G+3} until the stores have read it); the PV issuer
       // writes it out, clipping rows past N
