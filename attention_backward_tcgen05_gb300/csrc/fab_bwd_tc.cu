@@ -139,6 +139,7 @@ struct Params {
   const uint16_t* mask;
   float* dk;
   float* dv;
+  const int* qt_end;  // per key tile, one past the last query tile not all -inf in the mask; or null
 };
 
 template <int D, bool MASK, bool F16>
@@ -198,7 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int qt0 = p.causal ? x.m0 / C::BQ : 0;  // first query tile holding some n >= m0
     if (qt0 > q_tiles) qt0 = q_tiles;
     x.qt0 = qt0;
-    x.n_it = rk2 * (q_tiles - qt0);
+    int qt1 = q_tiles;  // one past the last query tile to visit
+    if constexpr (MASK) {
+      // query tiles past this one are all -inf in the mask: their P is 0
+      if (p.qt_end != nullptr && p.qt_end[jt] < qt1) qt1 = p.qt_end[jt];
+    }
+    x.n_it = qt1 > qt0 ? rk2 * (qt1 - qt0) : 0;
     return x;
   };
 
@@ -760,6 +766,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   p.mask = pr.mask;
   p.dk = pr.packed + pr.off_k / 4;
   p.dv = pr.packed + pr.off_v / 4;
+  p.qt_end = pr.qt_end;
   // persistent: one CTA per SM (each owns the SM's tensor memory), walking units
   const int64_t units = ((pr.M + C::BM - 1) / C::BM) * pr.Hkv * pr.B;
   int dev = 0, sms = 0;

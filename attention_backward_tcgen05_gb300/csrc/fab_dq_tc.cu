@@ -121,6 +121,7 @@ struct QParams {
   const uint16_t* o;  // forward output [D,H,N,B] (16-bit input type), read with FUSE_D
   float* pad[3];           // the packed result's padding after each slice, zeroed with FUSE_D
   int pad_n[3];
+  const int* kt_end;       // per query tile, one past the last key tile not all -inf in the mask; or null
 };
 
 template <int D, bool FUSE_D, bool F16>
@@ -174,6 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.causal) {
       const int last = (qt * C::BQ + C::BQ - 1) / C::BK + 1;  // key tiles holding some m <= n
       if (last < n_kv) n_kv = last;
+    }
+    if (p.kt_end != nullptr) {
+      // key tiles past this one are all -inf in the mask: their P is 0
+      const int e = p.kt_end[qt] > 1 ? p.kt_end[qt] : 1;
+      if (e < n_kv) n_kv = e;
     }
     x.nkv = n_kv;  // >= 1: key tile 0 holds m = 0 <= n
     return x;
@@ -726,6 +732,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   p.mask = pr.mask;
   p.dq = pr.packed;
   p.o = static_cast<const uint16_t*>(pr.o);
+  p.kt_end = pr.kt_end;
   {
     const int64_t nq = D * pr.N * pr.H * pr.B, nk = D * pr.M * pr.Hkv * pr.B;
     p.pad[0] = pr.packed + nq;

@@ -67,13 +67,37 @@ size_t di_bytes(const fab_dims* d) {
   return (b + 255) / 256 * 256;
 }
 
+// After D_i: the mask's per-tile bounds (an int per query tile and per key
+// tile), which let the tensor-core passes skip tiles whose mask entries are
+// all -inf.  Optional: a workspace without room for them skips nothing.
+size_t bounds_bytes(const fab_dims* d) {
+  const size_t b = (size_t)((d->N + 127) / 128 + (d->M + 127) / 128) * sizeof(int);
+  return (b + 255) / 256 * 256;
+}
+size_t aux_bytes(const fab_dims* d) { return di_bytes(d) + bounds_bytes(d); }
+
 // The forward output O [DV,H,N,B] and the row LSE [N,H,B] that fab_backward
-// keeps in its workspace, after D_i, when the caller passes neither.
+// keeps in its workspace, after D_i and the bounds, when the caller passes
+// neither.
 size_t o_bytes(const fab_dims* d, int dtype) {
   const size_t b = (size_t)(d->B * d->H * d->N * d->DV) * (dtype == FAB_F32 ? 4u : 2u);
   return (b + 255) / 256 * 256;
 }
-size_t recompute_bytes(const fab_dims* d, int dtype) { return di_bytes(d) + o_bytes(d, dtype) + di_bytes(d); }
+size_t recompute_bytes(const fab_dims* d, int dtype) { return aux_bytes(d) + o_bytes(d, dtype) + di_bytes(d); }
+
+// Points p's mask bounds into the workspace when there is a mask and room.
+void set_bounds(Problem* p, const fab_dims* d, const void* workspace, size_t workspace_bytes) {
+  p->kt_end = p->qt_end = nullptr;
+  if (p->mask == nullptr || workspace_bytes < aux_bytes(d)) return;
+  uint8_t* ws = static_cast<uint8_t*>(const_cast<void*>(workspace));
+  p->kt_end = reinterpret_cast<int*>(ws + di_bytes(d));
+  p->qt_end = p->kt_end + (d->N + 127) / 128;
+}
+
+// The bounds a tensor-core pass reads, computed on the stream before it.
+cudaError_t scan_bounds(const Problem& p, cudaStream_t s) {
+  return p.kt_end != nullptr ? launch_mask_bounds(p, s) : cudaSuccess;
+}
 
 Problem make_problem(const fab_dims* d, int dtype, float scale, int causal) {
   Problem p{};
@@ -158,7 +182,7 @@ FAB_API size_t fab_packed_bytes(const fab_dims* dims) {
 
 FAB_API size_t fab_backward_workspace_bytes(const fab_dims* dims, int dtype) {
   if (check_dims(dims) != FAB_OK || !dtype_ok(dtype)) return 0;
-  return di_bytes(dims);
+  return aux_bytes(dims);
 }
 
 FAB_API size_t fab_backward_recompute_workspace_bytes(const fab_dims* dims, int dtype) {
@@ -220,6 +244,9 @@ FAB_API int fab_backward_main(const void* q, const void* k, const void* v, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (backward_tc_supported(p)) {
     if (!encode_tiled_fn()) return FAB_ERR_CUDA;
+    set_bounds(&p, dims, workspace, workspace_bytes);
+    rc = from_cuda(scan_bounds(p, s));
+    if (rc != FAB_OK) return rc;
     // query pass (dQ), then key/value pass (dK, dV); they write disjoint slices
     rc = from_cuda(launch_dq_tc(p, false, s));
     if (rc != FAB_OK) return rc;
@@ -263,7 +290,11 @@ FAB_API int fab_backward_query_pass(const void* q, const void* k, const void* v,
   if (!tc_problem(q, k, v, d, o, lse, mask, causal, scale, dtype, dims, workspace, packed_out, &p))
     return FAB_ERR_UNSUPPORTED;
   if (!encode_tiled_fn()) return FAB_ERR_CUDA;
-  return from_cuda(launch_dq_tc(p, true, static_cast<cudaStream_t>(stream)));
+  set_bounds(&p, dims, workspace, workspace_bytes);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = from_cuda(scan_bounds(p, s));
+  if (rc != FAB_OK) return rc;
+  return from_cuda(launch_dq_tc(p, true, s));
 }
 
 FAB_API int fab_backward_key_pass(const void* q, const void* k, const void* v, const void* d, const float* lse,
@@ -278,7 +309,11 @@ FAB_API int fab_backward_key_pass(const void* q, const void* k, const void* v, c
                   packed_out, &p))
     return FAB_ERR_UNSUPPORTED;
   if (!encode_tiled_fn()) return FAB_ERR_CUDA;
-  return from_cuda(launch_backward_tc(p, static_cast<cudaStream_t>(stream)));
+  set_bounds(&p, dims, workspace, workspace_bytes);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = from_cuda(scan_bounds(p, s));
+  if (rc != FAB_OK) return rc;
+  return from_cuda(launch_backward_tc(p, s));
 }
 
 FAB_API int fab_backward(const void* q, const void* k, const void* v, const void* d, const void* o, const float* lse,
@@ -294,8 +329,8 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
     if (rc0 != FAB_OK) return rc0;
     if (workspace_bytes < recompute_bytes(dims, dtype)) return FAB_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    void* o2 = ws + di_bytes(dims);
-    float* lse2 = reinterpret_cast<float*>(ws + di_bytes(dims) + o_bytes(dims, dtype));
+    void* o2 = ws + aux_bytes(dims);
+    float* lse2 = reinterpret_cast<float*>(ws + aux_bytes(dims) + o_bytes(dims, dtype));
     rc0 = fab_forward_lse(q, k, v, mask, causal, scale, dtype, dims, o2, lse2, stream);
     if (rc0 != FAB_OK) return rc0;
     o = o2;
@@ -306,13 +341,17 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
   if (rc != FAB_OK) return rc;
   Problem p;
   if (tc_problem(q, k, v, d, o, lse, mask, causal, scale, dtype, dims, workspace, packed_out, &p)) {
-    // the query pass computes D_i itself (and zeroes the padding), then the
-    // key/value pass reads it: two launches, no preprocess
-    rc = fab_backward_query_pass(q, k, v, d, o, lse, mask, causal, scale, dtype, dims, workspace, workspace_bytes,
-                                 packed_out, stream);
+    // what fab_backward_query_pass then fab_backward_key_pass enqueue, with
+    // the mask's tile bounds scanned once: the query pass computes D_i itself
+    // (and zeroes the padding), then the key/value pass reads it
+    if (!encode_tiled_fn()) return FAB_ERR_CUDA;
+    set_bounds(&p, dims, workspace, workspace_bytes);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = from_cuda(scan_bounds(p, s));
     if (rc != FAB_OK) return rc;
-    return fab_backward_key_pass(q, k, v, d, lse, mask, causal, scale, dtype, dims, workspace, workspace_bytes,
-                                 packed_out, stream);
+    rc = from_cuda(launch_dq_tc(p, true, s));
+    if (rc != FAB_OK) return rc;
+    return from_cuda(launch_backward_tc(p, s));
   }
   rc = fab_backward_preprocess(d, o, dtype, dims, workspace, workspace_bytes, packed_out, stream);
   if (rc != FAB_OK) return rc;

@@ -27,6 +27,12 @@ struct Problem {
   const float* lse;
   const uint16_t* mask;  // f16 [M,N] or null
   float* di;             // workspace: D_i, f32 [N,H,B]
+  // workspace, only with a mask: per query tile, one past the last key tile
+  // holding a mask entry other than -inf (kt_end), and per key tile, one past
+  // the last such query tile (qt_end); tiles beyond them are skipped.  Null:
+  // no skipping.
+  int* kt_end;
+  int* qt_end;
   float* packed;         // packed f32 result
   size_t off_k, off_v, end;  // bytes
 };
@@ -35,11 +41,14 @@ struct Problem {
 // packed result.
 cudaError_t launch_preprocess(const Problem& p, cudaStream_t s);
 
+// fab_preprocess.cu: p.kt_end and p.qt_end from the mask (both non-null).
+cudaError_t launch_mask_bounds(const Problem& p, cudaStream_t s);
+
 // fab_simt.cu: CUDA-core kernels for every dtype and width (DK, DV <= 256).
 cudaError_t launch_forward_simt(const Problem& p, void* o, float* lse, cudaStream_t s);
 cudaError_t launch_backward_simt(const Problem& p, cudaStream_t s);
 
-// fab_fwd_tc.cu: the tcgen05 tensor-core forward with LSE (bf16, DK == DV in {64, 128}).
+// fab_fwd_tc.cu: the tcgen05 tensor-core forward with LSE (bf16 or f16, DK == DV in {64, 128}).
 bool forward_tc_supported(const Problem& p);
 cudaError_t launch_forward_tc(const Problem& p, void* o, float* lse, cudaStream_t s);
 

@@ -61,9 +61,15 @@ WORKLOADS = {
     "masked_nonsquare": Workload("masked_nonsquare", 8, 16, 4, 512, 8192, 128, 128, "bf16", "normal",
                                  1.0 / math.sqrt(128), mask="random", seed=1005,
                                  note="f16 mask [M,N]: 10% -inf, one query fully -inf, rest 0"),
+    # not one of the five: the gqa shape under a padding mask, where whole
+    # tiles of the mask are -inf (the tensor-core passes skip them)
+    "padded_d128": Workload("padded_d128", 4, 32, 8, 2048, 2048, 128, 128, "bf16", "normal",
+                            1.0 / math.sqrt(128), mask="pad", mask_p=0.05, seed=1006,
+                            note="f16 padding mask: keys from 5/8 M on and queries from 7/8 N on -inf, 5% -inf elsewhere"),
 }
 
 ORDER = ["tiny_f32", "causal_d64", "gqa_causal_d128", "long_seq", "masked_nonsquare"]
+EXTRA = ["padded_d128"]
 
 
 def custom(B, H, Hkv, N, M, DK, DV=None, dtype="bf16", dist="normal", scale=None, causal=False, mask="none",
@@ -106,6 +112,17 @@ def make(w: Workload, device="cpu"):
         mask[hit] = float("-inf")
         masked_query = int(torch.randint(0, N, (1,), generator=g).item())
         mask[masked_query, :] = float("-inf")
+        mask = mask.to(torch.float16)
+    elif w.mask == "pad":
+        # padding: keys from 5/8 M on and queries from 7/8 N on are -inf for
+        # everything (whole tiles of the mask then hold only -inf), plus
+        # Bernoulli(mask_p) -inf entries elsewhere
+        mv, nv = (M * 5) // 8 + 3, (N * 7) // 8 + 1
+        hit = torch.rand((N, M), generator=g, dtype=torch.float32) < w.mask_p
+        mask = torch.zeros((N, M), dtype=torch.float32)
+        mask[hit] = float("-inf")
+        mask[:, mv:] = float("-inf")
+        mask[nv:, :] = float("-inf")
         mask = mask.to(torch.float16)
     elif w.mask != "none":
         raise ValueError(w.mask)

@@ -104,13 +104,18 @@ FAB_EXPORT int fab_packed_offsets(const fab_dims* dims, size_t* off_k, size_t* o
 /* Total packed bytes (== end above), or 0 for bad dims. */
 FAB_EXPORT size_t fab_packed_bytes(const fab_dims* dims);
 
-/* Device workspace bytes fab_backward needs (holds D_i = rowsum(dO * O),
- * f32 [N,H,B]).  0 for bad dims. */
+/* Device workspace bytes fab_backward needs: D_i = rowsum(dO * O), f32
+ * [N,H,B], then, for a call with a mask, the mask's tile bounds (an int per
+ * 128-row query tile and per 128-key key tile: past them every mask entry is
+ * -inf, and the tensor-core passes skip those tiles; a workspace that ends
+ * after D_i skips nothing), each part a multiple of 256 bytes.  0 for bad
+ * dims. */
 FAB_EXPORT size_t fab_backward_workspace_bytes(const fab_dims* dims, int dtype);
 
 /* Device workspace bytes fab_backward needs when called without o and lse
- * (it then recomputes them): D_i, then O (`dtype`, [DV,H,N,B]) and LSE (f32,
- * [N,H,B]), each part a multiple of 256 bytes.  0 for bad dims. */
+ * (it then recomputes them): D_i and the tile bounds as above, then O
+ * (`dtype`, [DV,H,N,B]) and LSE (f32, [N,H,B]), each part a multiple of 256
+ * bytes.  0 for bad dims. */
 FAB_EXPORT size_t fab_backward_recompute_workspace_bytes(const fab_dims* dims, int dtype);
 
 /* Forward pass saving what the backward needs (labml "Flash Attention",

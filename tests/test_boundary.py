@@ -77,12 +77,15 @@ def test_workspace_bytes(L):
 
 
 def test_recompute_workspace_bytes(L):
-    # without o and lse: D_i, O (dtype) and LSE (f32), each rounded up to 256 bytes
+    # without o and lse: D_i, the mask's tile bounds (an int per query tile and
+    # per key tile), O (dtype) and LSE (f32), each rounded up to 256 bytes
     d = binding.make_dims(2, 4, 2, 100, 70, 64, 48)
     r256 = lambda x: (x + 255) // 256 * 256
     rows = 2 * 4 * 100
+    bounds = r256((1 + 1) * 4)
+    assert binding.fab_backward_workspace_bytes(d, binding.FAB_BF16) == r256(rows * 4) + bounds
     for dt, elem in ((binding.FAB_BF16, 2), (binding.FAB_F16, 2), (binding.FAB_F32, 4)):
-        want = r256(rows * 4) + r256(rows * 48 * elem) + r256(rows * 4)
+        want = r256(rows * 4) + bounds + r256(rows * 48 * elem) + r256(rows * 4)
         assert binding.fab_backward_recompute_workspace_bytes(d, dt) == want
         assert binding.fab_backward_recompute_workspace_bytes(d, dt) > binding.fab_backward_workspace_bytes(d, dt)
     assert binding.fab_backward_recompute_workspace_bytes(binding.make_dims(1, 3, 2, 1, 1, 1, 1), 1) == 0

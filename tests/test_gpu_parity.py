@@ -45,6 +45,12 @@ SMALL = [
     ("simt_f32_mask", 2, 2, 2, 33, 65, 64, 64, "f32", False, "random"),
     ("simt_bf16_odd", 1, 2, 1, 33, 47, 40, 24, "bf16", False, "random"),
     ("simt_f32_wide", 1, 1, 1, 20, 30, 256, 200, "f32", True, "none"),
+    # padding masks: whole tiles of -inf past the last live key / query tile
+    # are skipped (a query tile with no live key keeps one tile)
+    ("tc128_pad_mask_gqa", 2, 4, 2, 700, 900, 128, 128, "bf16", False, "pad"),
+    ("tc64_pad_mask_causal", 1, 2, 1, 700, 700, 64, 64, "bf16", True, "pad"),
+    ("tc128_pad_many_units", 8, 8, 4, 512, 1024, 128, 128, "bf16", False, "pad"),
+    ("tc128_f16_pad_mask", 2, 4, 2, 300, 600, 128, 128, "f16", True, "pad"),
     # float16 inputs: the tensor-core passes with f16 operands, the CUDA-core path
     ("tc128_f16_causal_gqa_mask", 2, 4, 2, 200, 300, 128, 128, "f16", True, "random"),
     ("tc64_f16_mask_ragged", 1, 4, 2, 96, 130, 64, 64, "f16", False, "random"),
@@ -134,10 +140,11 @@ FULL_SAMPLE = {
     "gqa_causal_d128": ([0, 13, 31], None),
     "long_seq": ([5], (16384 - 1024, 16384)),
     "masked_nonsquare": ([0, 9, 30], None),
+    "padded_d128": ([0, 13, 31], None),
 }
 
 
-@pytest.mark.parametrize("name", inputs.ORDER)
+@pytest.mark.parametrize("name", inputs.ORDER + inputs.EXTRA)
 def test_workload_parity(name):
     w = inputs.WORKLOADS[name]
     x = inputs.make(w)
