@@ -45,8 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (workload, pass); entries are removed when the kernel changes after the
 # capture.
 MEASURED_TRAFFIC = {
-    ("gqa_causal_d128", "query"): 253064704 + 98741248,
-    ("gqa_causal_d128", "key"): 309949184 + 38405888,
+    ("gqa_causal_d128", "query"): 254001664 + 98465280,
+    ("gqa_causal_d128", "key"): 311829760 + 37447168,
 }
 
 

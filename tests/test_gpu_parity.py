@@ -245,6 +245,32 @@ def test_backward_without_o_and_lse(case):
         assert errs[key] <= TOL[dtype], (key, errs)
 
 
+@pytest.mark.parametrize("D,dtype,causal", [(128, "bf16", False), (64, "bf16", True), (128, "f16", True)])
+def test_mask_tile_skipping_is_exact(D, dtype, causal):
+    # a tile whose mask entries are all -inf contributes P = 0 and dS = 0, so
+    # skipping it adds nothing that was not +0: with the tile bounds (the full
+    # workspace) and without them (a workspace that ends after D_i) the
+    # gradients agree bit for bit; the padding mask leaves whole tiles -inf
+    w = inputs.custom(2, 4, 2, 700, 900, D, D, dtype=dtype, causal=causal, mask="pad", mask_p=0.05, seed=83 + D)
+    x = inputs.make(w)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o, lse = binding.forward(g["q"], g["k"], g["v"], g["mask"], w.causal, w.scale)
+    dims = binding.dims_of(g["q"], g["k"], g["v"])
+    full = binding.fab_backward_workspace_bytes(dims, binding.dtype_code(g["q"]))
+    di_only = (w.B * w.H * w.N * 4 + 255) // 256 * 256
+    assert di_only < full
+    outs = []
+    for wsb in (full, di_only):
+        ws = torch.full((wsb,), 255, dtype=torch.uint8, device="cuda")
+        packed = torch.full((binding.fab_packed_bytes(dims) // 4,), float("nan"), device="cuda")
+        binding.fab_backward(g["q"], g["k"], g["v"], g["d"], o, lse, g["mask"], w.causal, w.scale, ws, packed)
+        outs.append(packed)
+    torch.cuda.synchronize()
+    assert binding.fab_last_device_error() == binding.FAB_OK
+    assert torch.equal(outs[0], outs[1])
+    assert not torch.isnan(outs[0]).any()
+
+
 @pytest.mark.parametrize("D,causal,mask", [(128, True, "none"), (64, False, "random"), (128, False, "random")])
 def test_two_phase_api_matches_fab_backward(D, causal, mask):
     # fab_backward_preprocess + fab_backward_main (D_i from the preprocess),
