@@ -94,7 +94,10 @@ struct Cfg {
   // the swizzled tiles need a 1024-byte-aligned base, checked at run time
   // (no room for alignment slack at D = 128); at least 116 KB so one CTA
   // owns an SM and its whole tensor memory
-  static constexpr uint32_t SMEM_USED = OFF_MISC + 64;
+  // the mask's query-tile spans of a CTA's first SPAN_CAP units
+  static constexpr int SPAN_CAP = 160;
+  static constexpr uint32_t OFF_SPAN = OFF_MISC + 64;
+  static constexpr uint32_t SMEM_USED = OFF_SPAN + SPAN_CAP * 4;
   static constexpr uint32_t SMEM = SMEM_USED > 118784 ? SMEM_USED : 118784;
   // tensor-memory columns: tile buffer b at 128 b (b = 0, 1)
   static constexpr uint32_t TM_X = 128, TM_DV = 256, TM_DK = 256 + D;
@@ -139,7 +142,7 @@ struct Params {
   const uint16_t* mask;
   float* dk;
   float* dv;
-  const int* qt_end;  // per key tile, one past the last query tile not all -inf in the mask; or null
+  const uint8_t* qt_live;  // per key tile, a byte per query tile: mask not all -inf there; or null
 };
 
 template <int D, bool MASK, bool F16>
@@ -183,6 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = m_tiles * hb;
   const int rk2 = (int)(p.H / p.Hkv);
   const int q_tiles = (int)((p.N + C::BQ - 1) / C::BQ);
+  uint32_t* span_s = reinterpret_cast<uint32_t*>(smem + C::OFF_SPAN);
+  const bool span_tab = MASK && p.qt_live != nullptr && q_tiles < 65536;
+  const int64_t live_qs = live_stride(q_tiles);
   struct Unit {
     int b, hkv, m0, qt0, n_it;
   };
@@ -190,20 +196,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = (int)gridDim.x, c = (int)blockIdx.x;
     return G * kk + ((kk & 1) ? G - 1 - c : c);
   };
-  auto unit_of = [&](int u) {
+  // the live spans of this CTA's first units' key tiles, found once here
+  // (made visible by the block sync below) instead of at every unit switch
+  // of every role: {first live query tile, one past the last} as 16-bit halves
+  if (span_tab)
+    for (int i = (int)threadIdx.x; i < C::SPAN_CAP && unit_at(i) < n_units; i += kThreads) {
+      int s0, s1;
+      live_span(p.qt_live + (unit_at(i) / hb) * live_qs, q_tiles, s0, s1);
+      span_s[i] = (uint32_t)s0 | ((uint32_t)s1 << 16);
+    }
+  // the unit this CTA takes in round kk; tab: its span from the shared table
+  // (filled before the block sync), else from the map itself
+  auto unit_of = [&](int kk, bool tab = true) {
     Unit x;
+    const int u = unit_at(kk);
     const int jt = u / hb, rem = u - jt * hb;
     x.b = rem / (int)p.Hkv;
     x.hkv = rem - x.b * (int)p.Hkv;
     x.m0 = jt * C::BM;
     int qt0 = p.causal ? x.m0 / C::BQ : 0;  // first query tile holding some n >= m0
     if (qt0 > q_tiles) qt0 = q_tiles;
-    x.qt0 = qt0;
     int qt1 = q_tiles;  // one past the last query tile to visit
     if constexpr (MASK) {
-      // query tiles past this one are all -inf in the mask: their P is 0
-      if (p.qt_end != nullptr && p.qt_end[jt] < qt1) qt1 = p.qt_end[jt];
+      // query tiles before the first and after the last live one are all
+      // -inf in the mask: their P is 0
+      // (a CTA's rounds past the table, if any, skip nothing)
+      if (span_tab && kk < C::SPAN_CAP) {
+        int s0, s1;
+        if (tab) {
+          const uint32_t v = span_s[kk];
+          s0 = (int)(v & 0xffffu);
+          s1 = (int)(v >> 16);
+        } else {
+          live_span(p.qt_live + jt * live_qs, q_tiles, s0, s1);
+        }
+        if (s0 > qt0) qt0 = s0;
+        if (s1 < qt1) qt1 = s1;
+      }
     }
+    x.qt0 = qt0;
     x.n_it = qt1 > qt0 ? rk2 * (qt1 - qt0) : 0;
     return x;
   };
@@ -240,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmO);
     for (int kk = 0; unit_at(kk) < n_units; ++kk) {
-      const Unit x = unit_of(unit_at(kk));
+      const Unit x = unit_of(kk, false);
       if (x.n_it == 0) continue;
       mbar_arrive_expect_tx(bar(B_KV), C::TILE);
       mbar_arrive_expect_tx(bar(B_V), C::TILE);
@@ -273,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0, ku = 0, q_issued = 0, o_issued = 0;
     int kv_issued = 0;  // the first unit's copies were started at barrier initialisation
     for (int kk = 0; kv_issued == 0 && unit_at(kk) < n_units; ++kk)
-      if (unit_of(unit_at(kk)).n_it > 0) kv_issued = 1;
+      if (unit_of(kk).n_it > 0) kv_issued = 1;
     int stG[3] = {-64, -64, -64}, stK[3] = {0, 0, 0};  // last tile and index of the latest units
     bool ok = true;
     // a load into the stage tile gg - dist left: wait for the staging of the
@@ -285,11 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     for (int kk = 0; ok && unit_at(kk) < n_units; ++kk) {
-      const Unit x = unit_of(unit_at(kk));
+      const Unit x = unit_of(kk);
       if (x.n_it == 0) continue;
       if (lane == 0)
         for (int k2 = kk + 1; unit_at(k2) < n_units; ++k2) {
-          const Unit y = unit_of(unit_at(k2));
+          const Unit y = unit_of(k2);
           if (y.n_it == 0) continue;
           for (int a = 0; a < C::ATOMS; ++a) {
             tma_prefetch_3d(&tmK, a * 64, y.m0, y.b * (int)p.Hkv + y.hkv);
@@ -416,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(B_S + (gg & 1)), issue);
       };
       for (int kk = 0; ok && unit_at(kk) < n_units; ++kk) {
-        const int n_it = unit_of(unit_at(kk)).n_it;
+        const int n_it = unit_of(kk).n_it;
         if (n_it == 0) continue;
         if (!(ok = wall(B_KV, ku & 1))) break;
         if (!(ok = wall(B_FQ + g % C::QST, (g / C::QST) & 1))) break;
@@ -454,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQ_mn = sdesc_sw128(sbase + C::OFF_Q, C::ATOM, 1024);
       auto p_col = [](int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); };
       for (int kk = 0; ok && unit_at(kk) < n_units; ++kk) {
-        const Unit x = unit_of(unit_at(kk));
+        const Unit x = unit_of(kk);
         if (x.n_it == 0) continue;
         for (int it = 0; it < x.n_it; ++it, ++g) {
           if (!(ok = wall(B_DS + (g & 1), (g >> 1) & 1))) break;
@@ -519,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t mk[MASK ? 32 : 1];
     int g = 0, ku = 0;
     for (int kk = 0; unit_at(kk) < n_units; ++kk) {
-      const Unit x = unit_of(unit_at(kk));
+      const Unit x = unit_of(kk);
       const int m = x.m0 + r;  // this thread's key (< 2^31)
       const bool key_in = m < p.M;
       if (x.n_it == 0) {
@@ -766,7 +797,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   p.mask = pr.mask;
   p.dk = pr.packed + pr.off_k / 4;
   p.dv = pr.packed + pr.off_v / 4;
-  p.qt_end = pr.qt_end;
+  p.qt_live = pr.qt_live;
   // persistent: one CTA per SM (each owns the SM's tensor memory), walking units
   const int64_t units = ((pr.M + C::BM - 1) / C::BM) * pr.Hkv * pr.B;
   int dev = 0, sms = 0;

@@ -411,4 +411,22 @@ FAB_DEV void st_shared_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// The first live tile and one past the last of a live-tile map row of n
+// bytes (16-byte aligned; the padding after n is ignored): first = n and
+// end = 0 when none is live.
+FAB_DEV void live_span(const uint8_t* row, int n, int& first, int& end) {
+  first = n;
+  end = 0;
+  for (int c = 0; c < n; c += 16) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + c));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (c + i < n && ((w[i >> 2] >> (8 * (i & 3))) & 0xffu) != 0u) {
+        if (first == n) first = c + i;
+        end = c + i + 1;
+      }
+  }
+}
+
 }  // namespace fab

@@ -76,7 +76,10 @@ struct QCfg {
   // +1024 to align the dynamic base; at least 116 KB so one CTA owns an SM
   // and its whole tensor memory
   static constexpr uint32_t OFF_DPART = OFF_MISC + 64;  // D_i partial sums, 2 x BQ floats
-  static constexpr uint32_t SMEM_USED = OFF_DPART + 2 * BQ * 4 + 1024;
+  // the mask's key-tile spans of a CTA's first SPAN_CAP units
+  static constexpr int SPAN_CAP = 160;
+  static constexpr uint32_t OFF_SPAN = OFF_DPART + 2 * BQ * 4;
+  static constexpr uint32_t SMEM_USED = OFF_SPAN + SPAN_CAP * 4 + 1024;
   static constexpr uint32_t SMEM = SMEM_USED > 118784 ? SMEM_USED : 118784;
   // tensor-memory columns
   static constexpr uint32_t TM_BUF = 128;  // buffer b at columns 128 b, b = 0, 1, 2
@@ -121,10 +124,10 @@ struct QParams {
   const uint16_t* o;  // forward output [D,H,N,B] (16-bit input type), read with FUSE_D
   float* pad[3];           // the packed result's padding after each slice, zeroed with FUSE_D
   int pad_n[3];
-  const int* kt_end;       // per query tile, one past the last key tile not all -inf in the mask; or null
+  const uint8_t* kt_live;  // per query tile, a byte per key tile: mask not all -inf there; or null
 };
 
-template <int D, bool FUSE_D, bool F16>
+template <int D, bool FUSE_D, bool F16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -155,15 +158,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hb = (int)(p.H * p.B);
   const int n_units = q_tiles * hb;
   const int H = (int)p.H, rk2 = (int)(p.H / p.Hkv), m_tiles = (int)((p.M + C::BK - 1) / C::BK);
+  uint32_t* span_s = reinterpret_cast<uint32_t*>(smem + C::OFF_SPAN);
+  const bool span_tab = MASK && p.kt_live != nullptr && m_tiles < 65536;
+  const int64_t live_ks = live_stride(m_tiles);
   struct Unit {
-    int h, b, hkv, n0, nkv;  // 32-bit; products that can exceed 2^31 widen first
+    int h, b, hkv, n0, j0, nkv;  // key tiles j0 .. j0 + nkv - 1; 32-bit, products that can exceed 2^31 widen first
   };
   auto unit_at = [&](int kk) {
     const int G = (int)gridDim.x, c = (int)blockIdx.x;
     return G * kk + ((kk & 1) ? G - 1 - c : c);
   };
-  auto unit_of = [&](int u) {
+  // the query tile of unit u
+  auto tile_of = [&](int u) {
+    const int qi = u / hb;
+    return p.causal ? q_tiles - 1 - qi : qi;
+  };
+  // the unit this CTA takes in round kk
+  auto unit_of = [&](int kk) {
     Unit x;
+    const int u = unit_at(kk);
     const int qi = u / hb, rem = u - qi * hb;
     const int b = rem / H, h = rem - b * H;
     x.h = h;
@@ -171,20 +184,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.hkv = h / rk2;
     const int qt = p.causal ? q_tiles - 1 - qi : qi;
     x.n0 = qt * C::BQ;
-    int n_kv = m_tiles;
+    int j0 = 0, j1 = m_tiles;
     if (p.causal) {
       const int last = (qt * C::BQ + C::BQ - 1) / C::BK + 1;  // key tiles holding some m <= n
-      if (last < n_kv) n_kv = last;
+      if (last < j1) j1 = last;
     }
-    if (p.kt_end != nullptr) {
-      // key tiles past this one are all -inf in the mask: their P is 0
-      const int e = p.kt_end[qt] > 1 ? p.kt_end[qt] : 1;
-      if (e < n_kv) n_kv = e;
+    if (MASK && span_tab && kk < C::SPAN_CAP) {
+      // key tiles before the first and after the last live one are all -inf
+      // in the mask: their P is 0 (a CTA's later rounds, if any, skip nothing)
+      const uint32_t v = span_s[kk];
+      const int s0 = (int)(v & 0xffffu), s1 = (int)(v >> 16);
+      if (s0 > j0) j0 = s0;
+      if (s1 < j1) j1 = s1;
+      if (j1 <= j0) j0 = 0, j1 = 1;  // nothing live: one tile (all P = 0), as without skipping
     }
-    x.nkv = n_kv;  // >= 1: key tile 0 holds m = 0 <= n
+    x.j0 = j0;
+    x.nkv = j1 - j0;  // >= 1: key tile 0 holds m = 0 <= n
     return x;
   };
 
+  // the live spans of this CTA's first units' query tiles, found once here
+  // (made visible by the block sync below) instead of at every unit switch
+  // of every role: {first live key tile, one past the last} as 16-bit halves
+  if (span_tab)
+    for (int i = (int)threadIdx.x; i < C::SPAN_CAP && unit_at(i) < n_units; i += kThreads) {
+      int s0, s1;
+      live_span(p.kt_live + tile_of(unit_at(i)) * live_ks, m_tiles, s0, s1);
+      span_s[i] = (uint32_t)s0 | ((uint32_t)s1 << 16);
+    }
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     *epi_cnt = 0u;
@@ -237,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stG[3] = {-8, -8, -8}, stK[3] = {0, 0, 0};  // last tile and index of the latest units
       bool ok = true;
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
-        const Unit x = unit_of(u);
+        const Unit x = unit_of(k);
         const int kvrow = (int)(x.b * p.Hkv + x.hkv);
         auto load_qo = [&]() {
           if (k > 0 && !(ok = mbar_wait(bar(Q_QOE), (k - 1) & 1, abort_flag, err))) return;
@@ -260,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int vs = g % C::VST;
           mbar_arrive_expect_tx(bar(Q_VF + vs), C::TILE);
           for (int a = 0; a < C::ATOMS; ++a)
-            tma_load_3d(sbase + C::OFF_V + vs * C::TILE + a * C::ATOM, &tmV, bar(Q_VF + vs), a * 64, j * C::BK,
-                        kvrow);
+            tma_load_3d(sbase + C::OFF_V + vs * C::TILE + a * C::ATOM, &tmV, bar(Q_VF + vs), a * 64,
+                        (x.j0 + j) * C::BK, kvrow);
           ++v_issued;
           // key stage g % 3 held K(g-3): free once dQ(g-3) finished, and
           // once any epilogue staging there has been stored
@@ -280,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ks = g % C::KST;
           mbar_arrive_expect_tx(bar(Q_KF + ks), C::TILE);
           for (int a = 0; a < C::ATOMS; ++a)
-            tma_load_3d(sbase + C::OFF_K + ks * C::TILE + a * C::ATOM, &tmK, bar(Q_KF + ks), a * 64, j * C::BK,
-                        kvrow);
+            tma_load_3d(sbase + C::OFF_K + ks * C::TILE + a * C::ATOM, &tmK, bar(Q_KF + ks), a * 64,
+                        (x.j0 + j) * C::BK, kvrow);
           ++k_issued;
         }
         if (ok && !qo) load_qo();
@@ -315,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQ_km = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
       const uint64_t dK_km = sdesc_sw128(sbase + C::OFF_K, 16, 1024);  // key stage 0, K-major
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
-        const int nkv = unit_of(u).nkv;
+        const int nkv = unit_of(k).nkv;
         if (!(ok = wall(Q_QF, k & 1))) break;
         // the previous unit's last dQ products go into the tensor pipe
         // before this unit's first scores: its epilogue waits for them
@@ -339,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dO_km = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
       const uint64_t dV_km = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
-        const int nkv = unit_of(u).nkv;
+        const int nkv = unit_of(k).nkv;
         if (!(ok = wall(Q_QF, k & 1))) break;
         if (k > 0 && !(ok = wall(Q_DQI, (k - 1) & 1))) break;  // as for the scores
         for (int j = 0; j < nkv; ++j, ++g) {
@@ -363,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dK_mn = sdesc_sw128(sbase + C::OFF_K, C::ATOM, 1024);
       auto a_col = [](int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); };
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
-        const int nkv = unit_of(u).nkv;
+        const int nkv = unit_of(k).nkv;
         for (int j = 0; j < nkv; ++j, ++g) {
           if (!(ok = wall(Q_DS + g % 3, (g / 3) & 1))) break;
           if (j == 0 && k > 0 && !(ok = wall(Q_DF, (k - 1) & 1))) break;
@@ -384,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // it out and release the two staging stages as each has been read
         if (!(ok = wall(Q_STG, k & 1))) break;
         if (lane == 0) {
-          const Unit x = unit_of(u);
+          const Unit x = unit_of(k);
           const int G = g - 1;
           const uint32_t st0 = sbase + C::OFF_K + (uint32_t)((G + 2) % 3) * C::TILE;  // columns 0 .. D/2-1
           const uint32_t st1 = sbase + C::OFF_K + (uint32_t)(G % 3) * C::TILE;        // columns D/2 .. D-1
@@ -411,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;  // query row within the tile
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c1 = p.scale * kLog2e;
-    const bool has_mask = p.mask != nullptr;
+    constexpr bool has_mask = MASK;
     const bool mvec = (p.M & 7) == 0;  // mask rows start 16-byte aligned
     float* dpart = reinterpret_cast<float*>(smem + C::OFF_DPART);
     if (FUSE_D && blockIdx.x == 0 && warp == 2 && lane == 0)
@@ -430,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (loads only, from a valid row: nothing here consumes a loaded value,
     // so the loads stay in flight; a row past N is masked where the values
     // are used)
-    auto fetch = [&](int uu) {
-      const Unit y = unit_of(uu);
+    auto fetch = [&](int kk) {
+      const Unit y = unit_of(kk);
       const int64_t ny = y.n0 + r < p.N ? y.n0 + r : p.N - 1;
       lse_next = ld_global_nc_f32(p.lse + (y.b * p.H + y.h) * p.N + ny);
       if (!FUSE_D) di_next = p.di[(y.b * p.H + y.h) * p.N + ny];
@@ -449,9 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     int g = 0, k = 0;
-    if (unit_at(0) < n_units) fetch(unit_at(0));
+    if (unit_at(0) < n_units) fetch(0);
     for (int u = unit_at(0); u < n_units; u = unit_at(++k)) {
-      const Unit x = unit_of(u);
+      const Unit x = unit_of(k);
       const int64_t n = x.n0 + r;
       const bool row_ok = n < p.N;
       const int64_t rowidx = (x.b * p.H + x.h) * p.N + (row_ok ? n : 0);
@@ -530,10 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if (has_mask && k == 0) load_mask(0);  // later units: fetched with the previous unit's tail
+      if (has_mask && k == 0) load_mask(x.j0);  // later units: fetched with the previous unit's tail
       bool ok = true;
-      int j = 0;
-      for (; j < x.nkv; ++j, ++g) {
+      int j = x.j0;
+      for (; j < x.j0 + x.nkv; ++j, ++g) {
         const uint32_t sb = (uint32_t)(g % 3) * C::TM_BUF, db = (uint32_t)((g + 2) % 3) * C::TM_BUF;
         const uint32_t ph = (uint32_t)(g / 3) & 1u;
         const int64_t m0 = (int64_t)j * C::BK;
@@ -558,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pv[2 * c] = fmaf(mf.x, kLog2e, pv[2 * c]);
             pv[2 * c + 1] = fmaf(mf.y, kLog2e, pv[2 * c + 1]);
           }
-          if (j + 1 < x.nkv) load_mask(j + 1);
+          if (j + 1 < x.j0 + x.nkv) load_mask(j + 1);
         }
         // keys past the causal diagonal (top-left: key m > query n) or past M;
         // only the diagonal tile and a ragged last tile have any
@@ -594,15 +621,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(Q_DS + g % 3));
       }
-      g += x.nkv - j;  // keep the tile count in step after an early exit
+      g += x.j0 + x.nkv - j;  // keep the tile count in step after an early exit
       if (unit_at(k + 1) < n_units) {
-        fetch(unit_at(k + 1));
+        fetch(k + 1);
         if (has_mask) {
-          const Unit y = unit_of(unit_at(k + 1));
+          const Unit y = unit_of(k + 1);
           const int64_t ny = y.n0 + r;
+          const int64_t my = (int64_t)y.j0 * C::BK + hf * 64;  // first key of the next unit's first tile
           if (ny < p.N) {
-            const uint16_t* src = p.mask + p.M * ny + hf * 64;
-            if (mvec && hf * 64 + 64 <= p.M) {
+            const uint16_t* src = p.mask + p.M * ny + my;
+            if (mvec && my + 64 <= p.M) {
               const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
@@ -615,8 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
-                const uint32_t lo = (hf * 64 + 2 * c < p.M) ? (uint32_t)__ldg(src + 2 * c) : 0u;
-                const uint32_t hi = (hf * 64 + 2 * c + 1 < p.M) ? (uint32_t)__ldg(src + 2 * c + 1) : 0u;
+                const uint32_t lo = (my + 2 * c < p.M) ? (uint32_t)__ldg(src + 2 * c) : 0u;
+                const uint32_t hi = (my + 2 * c + 1 < p.M) ? (uint32_t)__ldg(src + 2 * c + 1) : 0u;
                 mk[c] = lo | (hi << 16);
               }
             }
@@ -686,7 +714,7 @@ bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* di
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool FUSE_D, bool F16>
+template <int D, bool FUSE_D, bool F16, bool MASK>
 cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   using C = QCfg<D, F16>;
   const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -732,7 +760,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   p.mask = pr.mask;
   p.dq = pr.packed;
   p.o = static_cast<const uint16_t*>(pr.o);
-  p.kt_end = pr.kt_end;
+  p.kt_live = pr.kt_live;
   {
     const int64_t nq = D * pr.N * pr.H * pr.B, nk = D * pr.M * pr.Hkv * pr.B;
     p.pad[0] = pr.packed + nq;
@@ -749,21 +777,27 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const int64_t grid = units < sms ? units : sms;
   cudaError_t err =
-      cudaFuncSetAttribute(dq_tc_kernel<D, FUSE_D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      cudaFuncSetAttribute(dq_tc_kernel<D, FUSE_D, F16, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  dq_tc_kernel<D, FUSE_D, F16><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdq, p);
+  dq_tc_kernel<D, FUSE_D, F16, MASK><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdq, p);
   return cudaPeekAtLastError();
+}
+
+// the instance with the additive mask's code, or without it
+template <int D, bool FUSE_D, bool F16>
+cudaError_t launch_m(const Problem& pr, cudaStream_t s) {
+  return pr.mask != nullptr ? launch_d<D, FUSE_D, F16, true>(pr, s) : launch_d<D, FUSE_D, F16, false>(pr, s);
 }
 
 }  // namespace
 
 cudaError_t launch_dq_tc(const Problem& p, bool fuse_d, cudaStream_t s) {
   if (p.dtype == FAB_F16) {
-    if (fuse_d) return p.DK == 128 ? launch_d<128, true, true>(p, s) : launch_d<64, true, true>(p, s);
-    return p.DK == 128 ? launch_d<128, false, true>(p, s) : launch_d<64, false, true>(p, s);
+    if (fuse_d) return p.DK == 128 ? launch_m<128, true, true>(p, s) : launch_m<64, true, true>(p, s);
+    return p.DK == 128 ? launch_m<128, false, true>(p, s) : launch_m<64, false, true>(p, s);
   }
-  if (fuse_d) return p.DK == 128 ? launch_d<128, true, false>(p, s) : launch_d<64, true, false>(p, s);
-  return p.DK == 128 ? launch_d<128, false, false>(p, s) : launch_d<64, false, false>(p, s);
+  if (fuse_d) return p.DK == 128 ? launch_m<128, true, false>(p, s) : launch_m<64, true, false>(p, s);
+  return p.DK == 128 ? launch_m<128, false, false>(p, s) : launch_m<64, false, false>(p, s);
 }
 
 uint32_t take_error_dq() {

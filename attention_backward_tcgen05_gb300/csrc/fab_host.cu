@@ -67,11 +67,13 @@ size_t di_bytes(const fab_dims* d) {
   return (b + 255) / 256 * 256;
 }
 
-// After D_i: the mask's per-tile bounds (an int per query tile and per key
-// tile), which let the tensor-core passes skip tiles whose mask entries are
-// all -inf.  Optional: a workspace without room for them skips nothing.
+// After D_i: the mask's live-tile maps (a byte per 128 x 128 tile, by query
+// tile rows and by key tile rows), which let the tensor-core passes skip
+// tiles whose mask entries are all -inf.  Optional: a workspace without room
+// for them skips nothing.
 size_t bounds_bytes(const fab_dims* d) {
-  const size_t b = (size_t)((d->N + 127) / 128 + (d->M + 127) / 128) * sizeof(int);
+  const int64_t qt = (d->N + 127) / 128, kt = (d->M + 127) / 128;
+  const size_t b = (size_t)(qt * live_stride(kt) + kt * live_stride(qt));
   return (b + 255) / 256 * 256;
 }
 size_t aux_bytes(const fab_dims* d) { return di_bytes(d) + bounds_bytes(d); }
@@ -87,16 +89,17 @@ size_t recompute_bytes(const fab_dims* d, int dtype) { return aux_bytes(d) + o_b
 
 // Points p's mask bounds into the workspace when there is a mask and room.
 void set_bounds(Problem* p, const fab_dims* d, const void* workspace, size_t workspace_bytes) {
-  p->kt_end = p->qt_end = nullptr;
-  if (p->mask == nullptr || workspace_bytes < aux_bytes(d)) return;
+  p->kt_live = p->qt_live = nullptr;
+  // (the scan's grid holds up to 65535 query tiles)
+  if (p->mask == nullptr || workspace_bytes < aux_bytes(d) || (d->N + 127) / 128 > 65535) return;
   uint8_t* ws = static_cast<uint8_t*>(const_cast<void*>(workspace));
-  p->kt_end = reinterpret_cast<int*>(ws + di_bytes(d));
-  p->qt_end = p->kt_end + (d->N + 127) / 128;
+  p->kt_live = ws + di_bytes(d);
+  p->qt_live = p->kt_live + (d->N + 127) / 128 * live_stride((d->M + 127) / 128);
 }
 
 // The bounds a tensor-core pass reads, computed on the stream before it.
 cudaError_t scan_bounds(const Problem& p, cudaStream_t s) {
-  return p.kt_end != nullptr ? launch_mask_bounds(p, s) : cudaSuccess;
+  return p.kt_live != nullptr ? launch_mask_bounds(p, s) : cudaSuccess;
 }
 
 Problem make_problem(const fab_dims* d, int dtype, float scale, int causal) {

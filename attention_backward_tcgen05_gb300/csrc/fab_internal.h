@@ -27,12 +27,14 @@ struct Problem {
   const float* lse;
   const uint16_t* mask;  // f16 [M,N] or null
   float* di;             // workspace: D_i, f32 [N,H,B]
-  // workspace, only with a mask: per query tile, one past the last key tile
-  // holding a mask entry other than -inf (kt_end), and per key tile, one past
-  // the last such query tile (qt_end); tiles beyond them are skipped.  Null:
-  // no skipping.
-  int* kt_end;
-  int* qt_end;
+  // workspace, only with a mask: one byte per 128 x 128 tile of the mask,
+  // nonzero when the tile holds an entry other than -inf, stored twice:
+  // kt_live has a row per query tile over the key tiles, qt_live (right
+  // after it) a row per key tile over the query tiles, each row
+  // live_stride(tiles) bytes.  A pass skips the tiles before the first and
+  // after the last live tile of its row.  Null: no skipping.
+  uint8_t* kt_live;
+  uint8_t* qt_live;
   float* packed;         // packed f32 result
   size_t off_k, off_v, end;  // bytes
 };
@@ -41,7 +43,11 @@ struct Problem {
 // packed result.
 cudaError_t launch_preprocess(const Problem& p, cudaStream_t s);
 
-// fab_preprocess.cu: p.kt_end and p.qt_end from the mask (both non-null).
+// Bytes per row of a live-tile map over `tiles` tiles: padded to 16 so that
+// rows can be read in 16-byte pieces.
+__host__ __device__ inline int64_t live_stride(int64_t tiles) { return (tiles + 15) / 16 * 16; }
+
+// fab_preprocess.cu: p.kt_live and p.qt_live from the mask (both non-null).
 cudaError_t launch_mask_bounds(const Problem& p, cudaStream_t s);
 
 // fab_simt.cu: CUDA-core kernels for every dtype and width (DK, DV <= 256).

@@ -175,10 +175,12 @@ namespace {
 
 // One block per 128 x 128 (query tile, key tile) of the mask: does it hold an
 // entry other than -inf (f16 0xfc00)?  Entries outside the matrix do not
-// count.  Thread t reads 64 keys of row t / 2.
+// count.  Thread t reads 64 keys of row t / 2.  Every tile's byte is written
+// in both maps, so nothing has to be cleared first.
 __global__ void __launch_bounds__(256) mask_bounds_kernel(const uint16_t* __restrict__ mask, int64_t N, int64_t M,
-                                                          int* kt_end, int* qt_end) {
+                                                          uint8_t* kt_live, uint8_t* qt_live) {
   const int kt = (int)blockIdx.x, qt = (int)blockIdx.y;
+  const int64_t k_tiles = gridDim.x, q_tiles = gridDim.y;
   const int64_t n = (int64_t)qt * 128 + (threadIdx.x >> 1);
   const int64_t mb = (int64_t)kt * 128 + (threadIdx.x & 1) * 64;
   bool live = false;
@@ -197,9 +199,10 @@ __global__ void __launch_bounds__(256) mask_bounds_kernel(const uint16_t* __rest
       for (int e = 0; e < 64 && mb + e < M; ++e) live |= __ldg(row + mb + e) != 0xfc00u;
     }
   }
-  if (__syncthreads_or(live) && threadIdx.x == 0) {
-    atomicMax(kt_end + qt, kt + 1);
-    atomicMax(qt_end + kt, qt + 1);
+  const uint8_t any = __syncthreads_or(live) ? 1 : 0;
+  if (threadIdx.x == 0) {
+    kt_live[qt * live_stride(k_tiles) + kt] = any;
+    qt_live[kt * live_stride(q_tiles) + qt] = any;
   }
 }
 
@@ -207,11 +210,8 @@ __global__ void __launch_bounds__(256) mask_bounds_kernel(const uint16_t* __rest
 
 cudaError_t launch_mask_bounds(const Problem& p, cudaStream_t s) {
   const int64_t q_tiles = (p.N + 127) / 128, k_tiles = (p.M + 127) / 128;
-  // the two arrays are adjacent (qt_end follows kt_end): one fill
-  if (p.qt_end != p.kt_end + q_tiles) return cudaErrorInvalidValue;
-  cudaError_t err = cudaMemsetAsync(p.kt_end, 0, (size_t)(q_tiles + k_tiles) * sizeof(int), s);
-  if (err != cudaSuccess) return err;
-  mask_bounds_kernel<<<dim3((unsigned)k_tiles, (unsigned)q_tiles), 256, 0, s>>>(p.mask, p.N, p.M, p.kt_end, p.qt_end);
+  mask_bounds_kernel<<<dim3((unsigned)k_tiles, (unsigned)q_tiles), 256, 0, s>>>(p.mask, p.N, p.M, p.kt_live,
+                                                                              p.qt_live);
   return cudaPeekAtLastError();
 }
 

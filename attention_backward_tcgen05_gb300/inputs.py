@@ -34,12 +34,13 @@ class Workload:
     dist: str             # "uniform" (lo, hi) or "normal" (std)
     scale: float
     causal: bool = False
-    mask: str = "none"    # "none" | "random" (Bernoulli -inf with one fully masked query)
+    mask: str = "none"    # "none" | "random" (Bernoulli -inf with one fully masked query) | "pad" | "docs" | "band"
     mask_p: float = 0.1
     lo: float = -1.0
     hi: float = 1.0
     std: float = 1.0
     seed: int = 0
+    parts: int = 4        # "docs": number of documents; "band": half-width in 128-key tiles
     note: str = field(default="", compare=False)
 
     @property
@@ -66,17 +67,23 @@ WORKLOADS = {
     "padded_d128": Workload("padded_d128", 4, 32, 8, 2048, 2048, 128, 128, "bf16", "normal",
                             1.0 / math.sqrt(128), mask="pad", mask_p=0.05, seed=1006,
                             note="f16 padding mask: keys from 5/8 M on and queries from 7/8 N on -inf, 5% -inf elsewhere"),
+    # not one of the five either: the gqa shape with four packed documents
+    # (block-diagonal mask), where most tiles on both sides of each block are -inf
+    "docs_d128": Workload("docs_d128", 4, 32, 8, 2048, 2048, 128, 128, "bf16", "normal",
+                          1.0 / math.sqrt(128), mask="docs", mask_p=0.05, seed=1007, parts=4,
+                          note="f16 block-diagonal mask of 4 documents at random cuts, 5% -inf inside"),
 }
 
 ORDER = ["tiny_f32", "causal_d64", "gqa_causal_d128", "long_seq", "masked_nonsquare"]
-EXTRA = ["padded_d128"]
+EXTRA = ["padded_d128", "docs_d128"]
 
 
 def custom(B, H, Hkv, N, M, DK, DV=None, dtype="bf16", dist="normal", scale=None, causal=False, mask="none",
-           seed=0, std=1.0, lo=-1.0, hi=1.0, mask_p=0.1, name="custom") -> Workload:
+           seed=0, std=1.0, lo=-1.0, hi=1.0, mask_p=0.1, parts=4, name="custom") -> Workload:
     DV = DK if DV is None else DV
     scale = 1.0 / math.sqrt(DK) if scale is None else scale
-    return Workload(name, B, H, Hkv, N, M, DK, DV, dtype, dist, scale, causal, mask, mask_p, lo, hi, std, seed)
+    return Workload(name, B, H, Hkv, N, M, DK, DV, dtype, dist, scale, causal, mask, mask_p, lo, hi, std, seed,
+                    parts)
 
 
 def _draw(g, shape, w: Workload):
@@ -123,6 +130,25 @@ def make(w: Workload, device="cpu"):
         mask[hit] = float("-inf")
         mask[:, mv:] = float("-inf")
         mask[nv:, :] = float("-inf")
+        mask = mask.to(torch.float16)
+    elif w.mask in ("docs", "band"):
+        # Bernoulli(mask_p) -inf everywhere, then
+        # docs: `parts` documents cut at the same random fractions of N and M;
+        #   query n and key m see each other only inside one document
+        # band: key m is live for query n only within `parts` * 128 keys of
+        #   the scaled diagonal n * M / N
+        hit = torch.rand((N, M), generator=g, dtype=torch.float32) < w.mask_p
+        mask = torch.zeros((N, M), dtype=torch.float32)
+        mask[hit] = float("-inf")
+        n_idx = torch.arange(N, dtype=torch.float64)[:, None]
+        m_idx = torch.arange(M, dtype=torch.float64)[None, :]
+        if w.mask == "docs":
+            cuts = torch.sort(torch.rand((max(w.parts - 1, 0),), generator=g, dtype=torch.float64)).values
+            doc_n = torch.bucketize(n_idx / N, cuts, right=True)
+            doc_m = torch.bucketize(m_idx / M, cuts, right=True)
+            mask[doc_n != doc_m] = float("-inf")
+        else:
+            mask[(m_idx - n_idx * M / N).abs() > 128 * w.parts] = float("-inf")
         mask = mask.to(torch.float16)
     elif w.mask != "none":
         raise ValueError(w.mask)

@@ -77,13 +77,18 @@ def test_workspace_bytes(L):
 
 
 def test_recompute_workspace_bytes(L):
-    # without o and lse: D_i, the mask's tile bounds (an int per query tile and
-    # per key tile), O (dtype) and LSE (f32), each rounded up to 256 bytes
+    # without o and lse: D_i, the mask's live-tile maps (a byte per 128 x 128
+    # tile, rows per query tile and rows per key tile, each row padded to 16
+    # bytes), O (dtype) and LSE (f32), each rounded up to 256 bytes
     d = binding.make_dims(2, 4, 2, 100, 70, 64, 48)
     r256 = lambda x: (x + 255) // 256 * 256
+    r16 = lambda x: (x + 15) // 16 * 16
     rows = 2 * 4 * 100
-    bounds = r256((1 + 1) * 4)
+    bounds = r256(1 * r16(1) + 1 * r16(1))
     assert binding.fab_backward_workspace_bytes(d, binding.FAB_BF16) == r256(rows * 4) + bounds
+    # 40 query tiles x 24 key tiles: 40 rows of 32 bytes, 24 rows of 48
+    big = binding.make_dims(1, 2, 1, 5000, 3000, 128, 128)
+    assert binding.fab_backward_workspace_bytes(big, binding.FAB_BF16) == r256(2 * 5000 * 4) + r256(40 * 32 + 24 * 48)
     for dt, elem in ((binding.FAB_BF16, 2), (binding.FAB_F16, 2), (binding.FAB_F32, 4)):
         want = r256(rows * 4) + bounds + r256(rows * 48 * elem) + r256(rows * 4)
         assert binding.fab_backward_recompute_workspace_bytes(d, dt) == want

@@ -51,6 +51,16 @@ SMALL = [
     ("tc64_pad_mask_causal", 1, 2, 1, 700, 700, 64, 64, "bf16", True, "pad"),
     ("tc128_pad_many_units", 8, 8, 4, 512, 1024, 128, 128, "bf16", False, "pad"),
     ("tc128_f16_pad_mask", 2, 4, 2, 300, 600, 128, 128, "f16", True, "pad"),
+    # block-diagonal (documents) and banded (sliding window) masks: -inf tiles
+    # before and after each tile row's live span are skipped ("band:1": keys
+    # within 128 of the scaled diagonal)
+    ("tc128_docs_mask_gqa", 2, 4, 2, 900, 1100, 128, 128, "bf16", False, "docs:4"),
+    ("tc64_docs_mask_causal", 1, 2, 1, 1000, 1000, 64, 64, "bf16", True, "docs:3"),
+    ("tc128_band_mask", 1, 4, 4, 1000, 1000, 128, 128, "bf16", False, "band:1"),
+    ("tc128_band_causal_NltM", 2, 2, 1, 600, 1300, 128, 128, "bf16", True, "band:2"),
+    ("tc128_docs_many_units", 8, 8, 4, 640, 640, 128, 128, "bf16", False, "docs:5"),
+    ("tc128_f16_band_mask", 2, 4, 2, 700, 700, 128, 128, "f16", False, "band:1"),
+    ("simt_f32_docs", 1, 2, 1, 150, 170, 32, 32, "f32", False, "docs:3"),
     # float16 inputs: the tensor-core passes with f16 operands, the CUDA-core path
     ("tc128_f16_causal_gqa_mask", 2, 4, 2, 200, 300, 128, 128, "f16", True, "random"),
     ("tc64_f16_mask_ragged", 1, 4, 2, 96, 130, 64, 64, "f16", False, "random"),
@@ -65,8 +75,9 @@ SMALL = [
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
 def test_small_cases(case):
     name, B, H, Hkv, N, M, DK, DV, dtype, causal, mask = case
+    mask, _, parts = mask.partition(":")
     w = inputs.custom(B, H, Hkv, N, M, DK, DV, dtype=dtype, causal=causal, mask=mask, seed=zlib.crc32(name.encode()) % 1000,
-                      dist="uniform" if dtype == "f32" else "normal", name=name)
+                      dist="uniform" if dtype == "f32" else "normal", parts=int(parts or 4), name=name)
     x = inputs.make(w)
     gpu = run_gpu(w, x)
     ref = oracle_ref(w, x)
@@ -141,6 +152,7 @@ FULL_SAMPLE = {
     "long_seq": ([5], (16384 - 1024, 16384)),
     "masked_nonsquare": ([0, 9, 30], None),
     "padded_d128": ([0, 13, 31], None),
+    "docs_d128": ([0, 13, 31], None),
 }
 
 
@@ -245,13 +257,17 @@ def test_backward_without_o_and_lse(case):
         assert errs[key] <= TOL[dtype], (key, errs)
 
 
-@pytest.mark.parametrize("D,dtype,causal", [(128, "bf16", False), (64, "bf16", True), (128, "f16", True)])
-def test_mask_tile_skipping_is_exact(D, dtype, causal):
+@pytest.mark.parametrize("D,dtype,causal,mask,parts", [(128, "bf16", False, "pad", 4), (64, "bf16", True, "pad", 4),
+                                                       (128, "f16", True, "pad", 4), (128, "bf16", False, "docs", 4),
+                                                       (64, "bf16", True, "band", 1), (128, "bf16", False, "band", 2)])
+def test_mask_tile_skipping_is_exact(D, dtype, causal, mask, parts):
     # a tile whose mask entries are all -inf contributes P = 0 and dS = 0, so
-    # skipping it adds nothing that was not +0: with the tile bounds (the full
+    # skipping it adds nothing that was not +0: with the tile spans (the full
     # workspace) and without them (a workspace that ends after D_i) the
-    # gradients agree bit for bit; the padding mask leaves whole tiles -inf
-    w = inputs.custom(2, 4, 2, 700, 900, D, D, dtype=dtype, causal=causal, mask="pad", mask_p=0.05, seed=83 + D)
+    # gradients agree bit for bit; padding, document and band masks leave
+    # whole tiles -inf, after and before the live ones
+    w = inputs.custom(2, 4, 2, 700, 900, D, D, dtype=dtype, causal=causal, mask=mask, mask_p=0.05, seed=83 + D,
+                      parts=parts)
     x = inputs.make(w)
     g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     o, lse = binding.forward(g["q"], g["k"], g["v"], g["mask"], w.causal, w.scale)
