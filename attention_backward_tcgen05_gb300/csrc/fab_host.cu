@@ -345,7 +345,7 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
   Problem p;
   if (tc_problem(q, k, v, d, o, lse, mask, causal, scale, dtype, dims, workspace, packed_out, &p)) {
     // what fab_backward_query_pass then fab_backward_key_pass enqueue, with
-    // the mask's tile bounds scanned once: the query pass computes D_i itself
+    // the mask's live tiles scanned once: the query pass computes D_i itself
     // (and zeroes the padding), then the key/value pass reads it
     if (!encode_tiled_fn()) return FAB_ERR_CUDA;
     set_bounds(&p, dims, workspace, workspace_bytes);

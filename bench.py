@@ -45,8 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (workload, pass); entries are removed when the kernel changes after the
 # capture.
 MEASURED_TRAFFIC = {
-    ("gqa_causal_d128", "query"): 254001664 + 98465280,
-    ("gqa_causal_d128", "key"): 311829760 + 37447168,
+    ("gqa_causal_d128", "query"): 252111616 + 98254848,
+    ("gqa_causal_d128", "key"): 310495488 + 38434048,
 }
 
 
@@ -61,6 +61,34 @@ def pass_flops(w: inputs.Workload, gemms: int) -> float:
     dV, dK), halved for a causal mask."""
     f = 2.0 * gemms * w.B * w.H * w.N * w.M * w.DK
     return f / 2 if w.causal else f
+
+
+def executed_tile_fraction(w: inputs.Workload, mask, gemms: int) -> float:
+    """The share of its tiles a tensor-core pass runs when the mask's live
+    spans let it skip the rest: per row of 128 x 128 tiles (query tiles for
+    the query pass, gemms = 3; key tiles for the key pass, gemms = 4) the
+    tiles from the first to the last one holding an entry other than -inf,
+    within the causal bound; a query tile with none still runs one.  1.0
+    without a mask."""
+    if mask is None:
+        return 1.0
+    qt, kt = -(-w.N // 128), -(-w.M // 128)
+    live = torch.zeros((qt * 128, kt * 128), dtype=torch.bool)
+    live[:w.N, :w.M] = mask.float() != float("-inf")
+    live = live.reshape(qt, 128, kt, 128).any(3).any(1)
+    done = dense = 0
+    rows = live if gemms == 3 else live.t()
+    for i in range(rows.shape[0]):
+        if gemms == 3:
+            lo, hi = 0, (min(kt, (i * 128 + 127) // 128 + 1) if w.causal else kt)
+        else:
+            lo, hi = (min(qt, i) if w.causal else 0), qt
+        idx = torch.nonzero(rows[i]).flatten()
+        s0, s1 = (int(idx[0]), int(idx[-1]) + 1) if idx.numel() else (rows.shape[1], 0)
+        a, b = max(lo, s0), min(hi, s1)
+        done += (b - a) if b > a else (1 if gemms == 3 else 0)
+        dense += hi - lo
+    return done / dense if dense else 1.0
 
 
 def forward_flops(w: inputs.Workload) -> float:
@@ -411,11 +439,15 @@ def run_fab(args, rank, world, local):
             kname, kms, kflops, kkey = "dq_tc_kernel (query pass: S, dP, dQ, D_i)", first_mean, pass_flops(w, 3), "query"
     else:
         kname, kms, kflops, kkey = "dq_simt_kernel+dkdv_simt_kernel", second_mean, flops, None
+    # with a mask, only the tiles the kernel runs (the live spans) count
+    frac_run = executed_tile_fraction(w, xc["mask"], 4 if kkey == "key" else 3) if tensor_core else 1.0
+    kflops *= frac_run
     achieved = kflops / (kms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": args.traffic_bytes if args.traffic_bytes is not None else MEASURED_TRAFFIC.get((w.name, kkey)),
                 "kernel": kname, "kernel_ms": round(kms, 4), "kernel_flops": kflops,
+                "tiles_run": round(frac_run, 4),
                 "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone between L2 flushes)"}
 
     cpu = None

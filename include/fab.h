@@ -105,15 +105,16 @@ FAB_EXPORT int fab_packed_offsets(const fab_dims* dims, size_t* off_k, size_t* o
 FAB_EXPORT size_t fab_packed_bytes(const fab_dims* dims);
 
 /* Device workspace bytes fab_backward needs: D_i = rowsum(dO * O), f32
- * [N,H,B], then, for a call with a mask, the mask's tile bounds (an int per
- * 128-row query tile and per 128-key key tile: past them every mask entry is
- * -inf, and the tensor-core passes skip those tiles; a workspace that ends
- * after D_i skips nothing), each part a multiple of 256 bytes.  0 for bad
- * dims. */
+ * [N,H,B], then, for a call with a mask, the mask's live-tile maps (a byte
+ * per 128 x 128 tile, nonzero where some mask entry is not -inf, by query
+ * tile rows then by key tile rows, each row padded to 16 bytes; the
+ * tensor-core passes skip the tiles before the first and after the last live
+ * tile of each row, which changes no result bit; a workspace that ends after
+ * D_i skips nothing), each part a multiple of 256 bytes.  0 for bad dims. */
 FAB_EXPORT size_t fab_backward_workspace_bytes(const fab_dims* dims, int dtype);
 
 /* Device workspace bytes fab_backward needs when called without o and lse
- * (it then recomputes them): D_i and the tile bounds as above, then O
+ * (it then recomputes them): D_i and the live-tile maps as above, then O
  * (`dtype`, [DV,H,N,B]) and LSE (f32, [N,H,B]), each part a multiple of 256
  * bytes.  0 for bad dims. */
 FAB_EXPORT size_t fab_backward_recompute_workspace_bytes(const fab_dims* dims, int dtype);
