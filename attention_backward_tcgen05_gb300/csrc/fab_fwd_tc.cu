@@ -61,7 +61,10 @@ struct FCfg {
   // the swizzled tiles need a 1024-byte-aligned base, checked at run time
   // (no room for alignment slack at D = 128); at least 116 KB so one CTA
   // owns an SM and its whole tensor memory
-  static constexpr uint32_t SMEM_USED = OFF_MX + 2 * 2 * BQ * 4;
+  // the mask's key-tile spans of a CTA's first SPAN_CAP units
+  static constexpr int SPAN_CAP = 160;
+  static constexpr uint32_t OFF_SPAN = OFF_MX + 2 * 2 * BQ * 4;
+  static constexpr uint32_t SMEM_USED = OFF_SPAN + SPAN_CAP * 4;
   static constexpr uint32_t SMEM = SMEM_USED > 118784 ? SMEM_USED : 118784;
   static constexpr uint32_t TM_S = 0;  // + 128 * buffer, buffers 0..2
   static constexpr uint32_t TM_O = 384;
@@ -93,6 +96,7 @@ struct FParams {
   const uint16_t* mask;
   void* o;
   float* lse;
+  const uint8_t* kt_live;  // per query tile, a byte per key tile: mask not all -inf there; or null
 };
 
 template <int D, bool MASK, bool F16>
@@ -129,27 +133,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hb = (int)(p.H * p.B);
   const int n_units = q_tiles * hb;
   const int H = (int)p.H, rk2 = (int)(p.H / p.Hkv), m_tiles = (int)((p.M + C::BK - 1) / C::BK);
+  uint32_t* span_s = reinterpret_cast<uint32_t*>(smem + C::OFF_SPAN);
+  const bool span_tab = MASK && p.kt_live != nullptr && m_tiles < 65536;
+  const int64_t live_ks = live_stride(m_tiles);
   struct Unit {
-    int h, b, hkv, n0, nkv;
+    int h, b, hkv, n0, j0, nkv;  // key tiles j0 .. j0 + nkv - 1
   };
   auto unit_at = [&](int kk) {
     const int G = (int)gridDim.x, c = (int)blockIdx.x;
     return G * kk + ((kk & 1) ? G - 1 - c : c);
   };
-  auto unit_of = [&](int u) {
+  // the query tile of unit u
+  auto tile_of = [&](int u) {
+    const int qi = u / hb;
+    return p.causal ? q_tiles - 1 - qi : qi;
+  };
+  // the live spans of this CTA's first units' query tiles, found once here
+  // (made visible by the block sync below): {first live key tile, one past
+  // the last} as 16-bit halves
+  if (span_tab)
+    for (int i = (int)threadIdx.x; i < C::SPAN_CAP && unit_at(i) < n_units; i += kThreads) {
+      int s0, s1;
+      live_span(p.kt_live + tile_of(unit_at(i)) * live_ks, m_tiles, s0, s1);
+      span_s[i] = (uint32_t)s0 | ((uint32_t)s1 << 16);
+    }
+  // the unit this CTA takes in round kk
+  auto unit_of = [&](int kk) {
     Unit x;
+    const int u = unit_at(kk);
     const int qi = u / hb, rem = u - qi * hb;
     x.b = rem / H;
     x.h = rem - x.b * H;
     x.hkv = x.h / rk2;
     const int qt = p.causal ? q_tiles - 1 - qi : qi;
     x.n0 = qt * C::BQ;
-    int n_kv = m_tiles;
+    int j0 = 0, j1 = m_tiles;
     if (p.causal) {
       const int last = (x.n0 + C::BQ - 1) / C::BK + 1;  // key tiles holding some m <= n
-      if (last < n_kv) n_kv = last;
+      if (last < j1) j1 = last;
     }
-    x.nkv = n_kv;  // >= 1: key tile 0 holds m = 0 <= n
+    if (MASK && span_tab && kk < C::SPAN_CAP) {
+      // key tiles before the first and after the last live one are all -inf
+      // in the mask: they leave the running max, the row sum and O as they
+      // are (a CTA's later rounds, if any, skip nothing)
+      const uint32_t v = span_s[kk];
+      const int s0 = (int)(v & 0xffffu), s1 = (int)(v >> 16);
+      if (s0 > j0) j0 = s0;
+      if (s1 < j1) j1 = s1;
+      if (j1 <= j0) j0 = 0, j1 = 1;  // nothing live: one tile, as without skipping
+    }
+    x.j0 = j0;
+    x.nkv = j1 - j0;  // >= 1: key tile 0 holds m = 0 <= n
     return x;
   };
 
@@ -195,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stG[3] = {-8, -8, -8}, stK[3] = {0, 0, 0};  // last tile and index of the latest units
       bool ok = true;
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
-        const Unit x = unit_of(u);
+        const Unit x = unit_of(k);
         const int kvrow = x.b * (int)p.Hkv + x.hkv;
         for (int j = 0; j < x.nkv; ++j, ++g) {
           const int s = g % 3;
@@ -208,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(F_FULL + s), 2 * C::TILE);
           const uint32_t sk = sbase + C::OFF_KV + 2 * s * C::TILE;
           for (int a = 0; a < C::ATOMS; ++a) {
-            tma_load_3d(sk + a * C::ATOM, &tmK, bar(F_FULL + s), a * 64, j * C::BK, kvrow);
-            tma_load_3d(sk + C::TILE + a * C::ATOM, &tmV, bar(F_FULL + s), a * 64, j * C::BK, kvrow);
+            tma_load_3d(sk + a * C::ATOM, &tmK, bar(F_FULL + s), a * 64, (x.j0 + j) * C::BK, kvrow);
+            tma_load_3d(sk + C::TILE + a * C::ATOM, &tmV, bar(F_FULL + s), a * 64, (x.j0 + j) * C::BK, kvrow);
           }
           ++issued;
           if (j == 0) {
@@ -241,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sQ = sbase + C::OFF_Q;
       int g = 0, k = 0;
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
-        const int nkv = unit_of(u).nkv;
+        const int nkv = unit_of(k).nkv;
         if (!(ok = wall(F_Q, k & 1))) break;
         for (int j = 0; j < nkv; ++j, ++g) {
           const int s = g % 3;
@@ -269,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // with bulk tensor stores and releases the staging once they read it.
       int g = 0, k = 0;
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
-        const Unit x = unit_of(u);
+        const Unit x = unit_of(k);
         const int nkv = x.nkv;
         for (int j = 0; j < nkv; ++j, ++g) {
           const int s = g % 3;
@@ -314,14 +348,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int g = 0, k = 0;
     for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
-      const Unit x = unit_of(u);
+      const Unit x = unit_of(k);
       const int64_t n = (int64_t)x.n0 + r;
       const bool row_ok = n < p.N;
       const uint16_t* mrow = p.mask + p.M * (row_ok ? n : 0);
       float m_run = -INFINITY, l = 0.f;  // l: this half's share of the row sum
       for (int j = 0; j < x.nkv; ++j, ++g) {
         const int s = g % 3;
-        const int64_t m0 = (int64_t)j * C::BK;
+        const int64_t m0 = (int64_t)(x.j0 + j) * C::BK;
         const int64_t mb = m0 + hf * 64;  // first key of this thread's columns
         if (MASK) {
           // this thread's 64 mask values (f16 pairs); entries past M read as 0
@@ -550,6 +584,7 @@ cudaError_t launch_d(const Problem& pr, void* o, float* lse, cudaStream_t s) {
   p.mask = pr.mask;
   p.o = o;
   p.lse = lse;
+  p.kt_live = pr.kt_live;
   // persistent: one CTA per SM (each owns the SM's tensor memory), walking units
   const int64_t units = ((pr.N + C::BQ - 1) / C::BQ) * pr.H * pr.B;
   int dev = 0, sms = 0;

@@ -193,8 +193,12 @@ FAB_API size_t fab_backward_recompute_workspace_bytes(const fab_dims* dims, int 
   return recompute_bytes(dims, dtype);
 }
 
-FAB_API int fab_forward_lse(const void* q, const void* k, const void* v, const uint16_t* mask, int causal,
-                            float scale, int dtype, const fab_dims* dims, void* o, float* lse, fab_stream stream) {
+namespace {
+
+// fab_forward_lse; live: the mask's live-tile maps (scanned on the stream
+// before), which let the tensor-core forward skip all -inf tiles, or null.
+int forward_lse(const void* q, const void* k, const void* v, const uint16_t* mask, int causal, float scale,
+                int dtype, const fab_dims* dims, void* o, float* lse, const Problem* live, fab_stream stream) {
   int rc = check_dims(dims);
   if (rc != FAB_OK) return rc;
   if (!dtype_ok(dtype)) return FAB_ERR_INVALID;
@@ -208,12 +212,23 @@ FAB_API int fab_forward_lse(const void* q, const void* k, const void* v, const u
   p.k = k;
   p.v = v;
   p.mask = mask;
+  if (live != nullptr && mask != nullptr) {
+    p.kt_live = live->kt_live;
+    p.qt_live = live->qt_live;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (forward_tc_supported(p)) {
     if (!encode_tiled_fn()) return FAB_ERR_CUDA;
     return from_cuda(launch_forward_tc(p, o, lse, s));
   }
   return from_cuda(launch_forward_simt(p, o, lse, s));
+}
+
+}  // namespace
+
+FAB_API int fab_forward_lse(const void* q, const void* k, const void* v, const uint16_t* mask, int causal,
+                            float scale, int dtype, const fab_dims* dims, void* o, float* lse, fab_stream stream) {
+  return forward_lse(q, k, v, mask, causal, scale, dtype, dims, o, lse, nullptr, stream);
 }
 
 FAB_API int fab_backward_preprocess(const void* d, const void* o, int dtype, const fab_dims* dims, void* workspace,
@@ -322,6 +337,7 @@ FAB_API int fab_backward_key_pass(const void* q, const void* k, const void* v, c
 FAB_API int fab_backward(const void* q, const void* k, const void* v, const void* d, const void* o, const float* lse,
                          const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims,
                          void* workspace, size_t workspace_bytes, float* packed_out, fab_stream stream) {
+  bool scanned = false;  // the mask's live tiles already in the workspace
   if (o == nullptr || lse == nullptr) {
     // ggml_flash_attn_back's operands are q, k, v, the mask and d alone: with
     // neither o nor lse given, the forward is recomputed into the workspace
@@ -334,10 +350,17 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     void* o2 = ws + aux_bytes(dims);
     float* lse2 = reinterpret_cast<float*>(ws + aux_bytes(dims) + o_bytes(dims, dtype));
-    rc0 = fab_forward_lse(q, k, v, mask, causal, scale, dtype, dims, o2, lse2, stream);
+    // the mask's live tiles, scanned once for the forward and the backward
+    Problem live = make_problem(dims, dtype, scale, causal);
+    live.mask = mask;
+    set_bounds(&live, dims, workspace, workspace_bytes);
+    rc0 = from_cuda(scan_bounds(live, static_cast<cudaStream_t>(stream)));
+    if (rc0 != FAB_OK) return rc0;
+    rc0 = forward_lse(q, k, v, mask, causal, scale, dtype, dims, o2, lse2, &live, stream);
     if (rc0 != FAB_OK) return rc0;
     o = o2;
     lse = lse2;
+    scanned = true;
   }
   const void* ptrs[6] = {q, k, v, d, o, lse};
   int rc = check_backward(dims, dtype, ptrs, 6, mask, workspace, workspace_bytes, packed_out);
@@ -350,8 +373,10 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
     if (!encode_tiled_fn()) return FAB_ERR_CUDA;
     set_bounds(&p, dims, workspace, workspace_bytes);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    rc = from_cuda(scan_bounds(p, s));
-    if (rc != FAB_OK) return rc;
+    if (!scanned) {
+      rc = from_cuda(scan_bounds(p, s));
+      if (rc != FAB_OK) return rc;
+    }
     rc = from_cuda(launch_dq_tc(p, true, s));
     if (rc != FAB_OK) return rc;
     return from_cuda(launch_backward_tc(p, s));

@@ -225,14 +225,20 @@ def test_every_slice_written_over_garbage(D, causal, mask):
 
 
 @pytest.mark.parametrize("case", [("tc128_gqa_causal", 2, 4, 2, 200, 300, 128, 128, "bf16", True, "random"),
-                                  ("simt_f32", 1, 2, 1, 40, 50, 16, 24, "f32", True, "none")], ids=lambda c: c[0])
+                                  ("simt_f32", 1, 2, 1, 40, 50, 16, 24, "f32", True, "none"),
+                                  # the recomputed forward skips the mask's all -inf tiles too
+                                  ("tc128_docs", 2, 4, 2, 700, 900, 128, 128, "bf16", False, "docs:4"),
+                                  ("tc64_pad_causal", 1, 2, 1, 700, 700, 64, 64, "bf16", True, "pad:4"),
+                                  ("tc128_f16_band", 2, 4, 2, 600, 600, 128, 128, "f16", False, "band:1")],
+                         ids=lambda c: c[0])
 def test_backward_without_o_and_lse(case):
     # o and lse NULL: the library recomputes the forward into the workspace;
     # the result is the explicit forward-then-backward result, bit for bit,
     # and meets the oracle at the usual tolerance
     name, B, H, Hkv, N, M, DK, DV, dtype, causal, mask = case
+    mask, _, parts = mask.partition(":")
     w = inputs.custom(B, H, Hkv, N, M, DK, DV, dtype=dtype, causal=causal, mask=mask, seed=71,
-                      dist="uniform" if dtype == "f32" else "normal", name=name)
+                      dist="uniform" if dtype == "f32" else "normal", parts=int(parts or 4), name=name)
     x = inputs.make(w)
     g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     o, lse = binding.forward(g["q"], g["k"], g["v"], g["mask"], w.causal, w.scale)
@@ -248,6 +254,15 @@ def test_backward_without_o_and_lse(case):
     binding.fab_backward(g["q"], g["k"], g["v"], g["d"], None, None, g["mask"], w.causal, w.scale, ws, packed)
     torch.cuda.synchronize()
     assert torch.equal(packed, explicit)
+    # the O and LSE it recomputed (after D_i and the mask's live-tile maps)
+    # are the forward's own, bit for bit
+    aux = binding.fab_backward_workspace_bytes(dims, binding.dtype_code(g["q"]))
+    ob = o.numel() * o.element_size()
+    o_ws = ws[aux:aux + ob].view(o.dtype).view(o.shape)
+    lse_at = aux + (ob + 255) // 256 * 256
+    lse_ws = ws[lse_at:lse_at + lse.numel() * 4].view(torch.float32).view(lse.shape)
+    assert torch.equal(o_ws, o)
+    assert torch.equal(lse_ws, lse)
     ref = oracle_ref(w, x)
     f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
     dq, dk, dv = binding.unpack(recomputed, dims)
