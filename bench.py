@@ -91,6 +91,17 @@ def executed_tile_fraction(w: inputs.Workload, mask, gemms: int) -> float:
     return done / dense if dense else 1.0
 
 
+def preprocess_bytes(w: inputs.Workload) -> int:
+    """Algorithmic DRAM bytes of the D_i kernel: dO and O read once (the input
+    type), D_i written (f32), the packed result's padding zeroed."""
+    elem = 4 if w.dtype == "f32" else 2
+    rows = w.B * w.H * w.N
+    pad16 = lambda n: (n + 3) // 4 * 4  # floats, to 16 bytes
+    nq, nk, nv = rows * w.DK, w.B * w.Hkv * w.M * w.DK, w.B * w.Hkv * w.M * w.DV
+    pad = (pad16(nq) - nq) + (pad16(nk) - nk) + (pad16(nv) - nv)
+    return 2 * rows * w.DV * elem + rows * 4 + pad * 4
+
+
 def forward_flops(w: inputs.Workload) -> float:
     f = 4.0 * w.B * w.H * w.N * w.M * w.DK
     return f / 2 if w.causal else f
@@ -291,6 +302,20 @@ def run_fab(args, rank, world, local):
                 rec_ms.append(e0.elapsed_time(e1))
         del ws_r, packed_r, flush_r
 
+    # the two-phase API's D_i kernel (fab_backward computes D_i inside the
+    # query pass instead): HBM-bound, timed on its own between L2 flushes
+    pre_ms = []
+    if args.forward_steps:
+        for i in range(4):
+            flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            binding.fab_backward_preprocess(d, o, dims, ws, packed)
+            e1.record(stream)
+            e1.synchronize()
+            if i > 0:
+                pre_ms.append(e0.elapsed_time(e1))
+
     # the two launches of one backward step (what fab_backward enqueues)
     if tensor_core:
         stage_names = ("query_pass", "key_pass")
@@ -475,6 +500,14 @@ def run_fab(args, rank, world, local):
                          "ms": round(statistics.median(fwd_ms), 3),
                          "kernel": "fwd_tc_kernel" if tensor_core else "fwd_simt_kernel"}
                         if fwd_ms else None),
+            "preprocess": ({"gbps": round(preprocess_bytes(w) / (statistics.median(pre_ms) / 1e3) / 1e9, 1),
+                            "ms": round(statistics.median(pre_ms), 4), "bytes": preprocess_bytes(w),
+                            "peak_gbps": float(peaks["hbm_gbs"]),
+                            "frac": round(preprocess_bytes(w) / (statistics.median(pre_ms) / 1e3) / 1e9
+                                          / float(peaks["hbm_gbs"]), 4),
+                            "kernel": "preprocess_kernel (fab_backward_preprocess: D_i and the packed padding)",
+                            "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
+                           if pre_ms else None),
             "recompute": ({"ms": round(statistics.median(rec_ms), 3),
                            "tflops_fwd_plus_bwd": round((forward_flops(w) + flops) / (statistics.median(rec_ms) / 1e3)
                                                         / 1e12, 2),
