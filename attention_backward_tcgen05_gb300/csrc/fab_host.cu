@@ -71,15 +71,15 @@ size_t di_bytes(const fab_dims* d) {
 // tile rows and by key tile rows), which let the tensor-core passes skip
 // tiles whose mask entries are all -inf.  Optional: a workspace without room
 // for them skips nothing.
-size_t bounds_bytes(const fab_dims* d) {
+size_t live_map_bytes(const fab_dims* d) {
   const int64_t qt = (d->N + 127) / 128, kt = (d->M + 127) / 128;
   const size_t b = (size_t)(qt * live_stride(kt) + kt * live_stride(qt));
   return (b + 255) / 256 * 256;
 }
-size_t aux_bytes(const fab_dims* d) { return di_bytes(d) + bounds_bytes(d); }
+size_t aux_bytes(const fab_dims* d) { return di_bytes(d) + live_map_bytes(d); }
 
 // The forward output O [DV,H,N,B] and the row LSE [N,H,B] that fab_backward
-// keeps in its workspace, after D_i and the bounds, when the caller passes
+// keeps in its workspace, after D_i and the live-tile maps, when the caller passes
 // neither.
 size_t o_bytes(const fab_dims* d, int dtype) {
   const size_t b = (size_t)(d->B * d->H * d->N * d->DV) * (dtype == FAB_F32 ? 4u : 2u);
@@ -87,8 +87,8 @@ size_t o_bytes(const fab_dims* d, int dtype) {
 }
 size_t recompute_bytes(const fab_dims* d, int dtype) { return aux_bytes(d) + o_bytes(d, dtype) + di_bytes(d); }
 
-// Points p's mask bounds into the workspace when there is a mask and room.
-void set_bounds(Problem* p, const fab_dims* d, const void* workspace, size_t workspace_bytes) {
+// Points p's live-tile maps into the workspace when there is a mask and room.
+void set_live_maps(Problem* p, const fab_dims* d, const void* workspace, size_t workspace_bytes) {
   p->kt_live = p->qt_live = nullptr;
   // (the scan's grid holds up to 65535 query tiles)
   if (p->mask == nullptr || workspace_bytes < aux_bytes(d) || (d->N + 127) / 128 > 65535) return;
@@ -97,9 +97,9 @@ void set_bounds(Problem* p, const fab_dims* d, const void* workspace, size_t wor
   p->qt_live = p->kt_live + (d->N + 127) / 128 * live_stride((d->M + 127) / 128);
 }
 
-// The bounds a tensor-core pass reads, computed on the stream before it.
-cudaError_t scan_bounds(const Problem& p, cudaStream_t s) {
-  return p.kt_live != nullptr ? launch_mask_bounds(p, s) : cudaSuccess;
+// The live-tile maps the tensor-core passes read, written on the stream before them.
+cudaError_t scan_live_tiles(const Problem& p, cudaStream_t s) {
+  return p.kt_live != nullptr ? launch_mask_scan(p, s) : cudaSuccess;
 }
 
 Problem make_problem(const fab_dims* d, int dtype, float scale, int causal) {
@@ -262,8 +262,8 @@ FAB_API int fab_backward_main(const void* q, const void* k, const void* v, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (backward_tc_supported(p)) {
     if (!encode_tiled_fn()) return FAB_ERR_CUDA;
-    set_bounds(&p, dims, workspace, workspace_bytes);
-    rc = from_cuda(scan_bounds(p, s));
+    set_live_maps(&p, dims, workspace, workspace_bytes);
+    rc = from_cuda(scan_live_tiles(p, s));
     if (rc != FAB_OK) return rc;
     // query pass (dQ), then key/value pass (dK, dV); they write disjoint slices
     rc = from_cuda(launch_dq_tc(p, false, s));
@@ -308,9 +308,9 @@ FAB_API int fab_backward_query_pass(const void* q, const void* k, const void* v,
   if (!tc_problem(q, k, v, d, o, lse, mask, causal, scale, dtype, dims, workspace, packed_out, &p))
     return FAB_ERR_UNSUPPORTED;
   if (!encode_tiled_fn()) return FAB_ERR_CUDA;
-  set_bounds(&p, dims, workspace, workspace_bytes);
+  set_live_maps(&p, dims, workspace, workspace_bytes);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = from_cuda(scan_bounds(p, s));
+  rc = from_cuda(scan_live_tiles(p, s));
   if (rc != FAB_OK) return rc;
   return from_cuda(launch_dq_tc(p, true, s));
 }
@@ -327,9 +327,9 @@ FAB_API int fab_backward_key_pass(const void* q, const void* k, const void* v, c
                   packed_out, &p))
     return FAB_ERR_UNSUPPORTED;
   if (!encode_tiled_fn()) return FAB_ERR_CUDA;
-  set_bounds(&p, dims, workspace, workspace_bytes);
+  set_live_maps(&p, dims, workspace, workspace_bytes);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = from_cuda(scan_bounds(p, s));
+  rc = from_cuda(scan_live_tiles(p, s));
   if (rc != FAB_OK) return rc;
   return from_cuda(launch_backward_tc(p, s));
 }
@@ -353,8 +353,8 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
     // the mask's live tiles, scanned once for the forward and the backward
     Problem live = make_problem(dims, dtype, scale, causal);
     live.mask = mask;
-    set_bounds(&live, dims, workspace, workspace_bytes);
-    rc0 = from_cuda(scan_bounds(live, static_cast<cudaStream_t>(stream)));
+    set_live_maps(&live, dims, workspace, workspace_bytes);
+    rc0 = from_cuda(scan_live_tiles(live, static_cast<cudaStream_t>(stream)));
     if (rc0 != FAB_OK) return rc0;
     rc0 = forward_lse(q, k, v, mask, causal, scale, dtype, dims, o2, lse2, &live, stream);
     if (rc0 != FAB_OK) return rc0;
@@ -371,10 +371,10 @@ FAB_API int fab_backward(const void* q, const void* k, const void* v, const void
     // the mask's live tiles scanned once: the query pass computes D_i itself
     // (and zeroes the padding), then the key/value pass reads it
     if (!encode_tiled_fn()) return FAB_ERR_CUDA;
-    set_bounds(&p, dims, workspace, workspace_bytes);
+    set_live_maps(&p, dims, workspace, workspace_bytes);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!scanned) {
-      rc = from_cuda(scan_bounds(p, s));
+      rc = from_cuda(scan_live_tiles(p, s));
       if (rc != FAB_OK) return rc;
     }
     rc = from_cuda(launch_dq_tc(p, true, s));

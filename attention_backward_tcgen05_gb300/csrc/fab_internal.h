@@ -48,7 +48,7 @@ cudaError_t launch_preprocess(const Problem& p, cudaStream_t s);
 __host__ __device__ inline int64_t live_stride(int64_t tiles) { return (tiles + 15) / 16 * 16; }
 
 // fab_preprocess.cu: p.kt_live and p.qt_live from the mask (both non-null).
-cudaError_t launch_mask_bounds(const Problem& p, cudaStream_t s);
+cudaError_t launch_mask_scan(const Problem& p, cudaStream_t s);
 
 // fab_simt.cu: CUDA-core kernels for every dtype and width (DK, DV <= 256).
 cudaError_t launch_forward_simt(const Problem& p, void* o, float* lse, cudaStream_t s);

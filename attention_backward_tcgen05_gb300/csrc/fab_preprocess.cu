@@ -177,7 +177,7 @@ namespace {
 // entry other than -inf (f16 0xfc00)?  Entries outside the matrix do not
 // count.  Thread t reads 64 keys of row t / 2.  Every tile's byte is written
 // in both maps, so nothing has to be cleared first.
-__global__ void __launch_bounds__(256) mask_bounds_kernel(const uint16_t* __restrict__ mask, int64_t N, int64_t M,
+__global__ void __launch_bounds__(256) mask_live_kernel(const uint16_t* __restrict__ mask, int64_t N, int64_t M,
                                                           uint8_t* kt_live, uint8_t* qt_live) {
   const int kt = (int)blockIdx.x, qt = (int)blockIdx.y;
   const int64_t k_tiles = gridDim.x, q_tiles = gridDim.y;
@@ -208,9 +208,9 @@ __global__ void __launch_bounds__(256) mask_bounds_kernel(const uint16_t* __rest
 
 }  // namespace
 
-cudaError_t launch_mask_bounds(const Problem& p, cudaStream_t s) {
+cudaError_t launch_mask_scan(const Problem& p, cudaStream_t s) {
   const int64_t q_tiles = (p.N + 127) / 128, k_tiles = (p.M + 127) / 128;
-  mask_bounds_kernel<<<dim3((unsigned)k_tiles, (unsigned)q_tiles), 256, 0, s>>>(p.mask, p.N, p.M, p.kt_live,
+  mask_live_kernel<<<dim3((unsigned)k_tiles, (unsigned)q_tiles), 256, 0, s>>>(p.mask, p.N, p.M, p.kt_live,
                                                                               p.qt_live);
   return cudaPeekAtLastError();
 }
