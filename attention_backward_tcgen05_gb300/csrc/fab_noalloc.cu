@@ -2,7 +2,8 @@
 // cannot allocate device memory.
 //
 // fab_backward needs a small device workspace (the per-row D_i terms, 4 bytes
-// per query row and head).  Some callers cannot provide one: code whose
+// per query row and head, and with a mask its live-tile maps, a byte per
+// 128 x 128 tile twice).  Some callers cannot provide one: code whose
 // device memory belongs to another allocator that it may not bypass, or code
 // that must not call cudaMalloc on its path because cudaMalloc can
 // synchronise the device and stall other streams.  This entry point keeps that
@@ -15,7 +16,9 @@
 // current, on the first call there.  All calls on a device share the array:
 // two calls whose work overlaps on the GPU (different streams, no ordering
 // between them) race on it.  Nothing in it has to start at zero: each call
-// overwrites every D_i entry it reads before reading it.
+// overwrites every D_i entry and map byte it reads before reading it.  When
+// the maps do not fit after D_i, the call runs without them (every tile of
+// a masked problem is computed; same results).
 #include <mutex>
 
 #include "fab.h"
@@ -53,7 +56,7 @@ extern "C" FAB_EXPORT int fab_backward_noalloc(const void* q, const void* k, con
                                                float scale, int dtype, const fab_dims* dims, float* packed_out,
                                                fab_stream stream) {
   if (dims == nullptr || dims->B <= 0 || dims->H <= 0 || dims->N <= 0) return FAB_ERR_INVALID;
-  if (o == nullptr || lse == nullptr) return FAB_ERR_INVALID;  // the fixed scratch holds D_i only
+  if (o == nullptr || lse == nullptr) return FAB_ERR_INVALID;  // no room for a recomputed O and LSE
   // B*H*N rows of D_i must fit the fixed array (checked without overflow)
   if (dims->B > fab::kMaxRows || dims->H > fab::kMaxRows / dims->B || dims->N > fab::kMaxRows / (dims->B * dims->H))
     return FAB_ERR_WORKSPACE;

@@ -184,7 +184,8 @@ FAB_EXPORT int fab_backward_key_pass(const void* q, const void* k, const void* v
 #define FAB_NOALLOC_MAX_ROWS 1048576
 
 /* fab_backward for callers that cannot allocate device memory (o and lse
- * must be given: the fixed scratch holds D_i only), for example
+ * must be given: the fixed scratch holds D_i and, when they fit after it, the
+ * mask's live-tile maps, not a recomputed O and LSE), for example
  * code whose device memory belongs to another allocator, or code that must not
  * call cudaMalloc (which can synchronise the device) on its path.  The pages
  * have no counterpart; the operation and every argument are those of

@@ -148,7 +148,7 @@ def test_recompute_validation(L):
     assert call_backward(L, binding.make_dims(1, 3, 2, 4, 4, 8, 8), none, ws_bytes=big) == binding.FAB_ERR_INVALID
     vp = ctypes.c_void_p
     args = [vp(FAKE)] * 4 + [None, None, None, 0, 1.0, 1, ctypes.byref(d), vp(FAKE), None]
-    assert L.fab_backward_noalloc(*args) == binding.FAB_ERR_INVALID  # its scratch holds D_i only
+    assert L.fab_backward_noalloc(*args) == binding.FAB_ERR_INVALID  # no room for a recomputed O and LSE
 
 
 def test_unsupported_width(L):
