@@ -338,6 +338,12 @@ def run_fab(args, rank, world, local):
         first()
         second()
 
+    # kernels one step launches: the query pass and the key/value pass, each
+    # entry point with a mask also scanning it (fab_backward itself scans once
+    # for both); on the CUDA-core path the D_i kernel, then dq_simt and
+    # dkdv_simt
+    launches_per_step = (2 + (2 if mask is not None else 0)) if tensor_core else 3
+
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -492,7 +498,7 @@ def run_fab(args, rank, world, local):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * args.steps,  # two kernels per step (see stages_ms)
+            "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "stages_ms": {stage_names[0]: round(first_mean, 4), stage_names[1]: round(second_mean, 4)},
             "wall_s": round(wall, 4),
