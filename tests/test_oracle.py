@@ -303,6 +303,37 @@ def test_gqa_equals_group_sum_of_mha():
     np.testing.assert_allclose(g["dv"], m["dv"].reshape(B, Hkv, rk2, M, D).sum(2), rtol=1e-12, atol=1e-14)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_diagonal_mask_splits_into_documents(causal):
+    # with -inf between documents (a block-diagonal mask), attention over the
+    # whole sequence is attention over each document alone: every row of O,
+    # LSE and dQ, and every row of dK and dV, equals the one-document run's.
+    # Finite mask values inside the documents take part.  Causal: the
+    # documents start at the same index on both axes, so the top-left
+    # diagonal inside a document is the document's own.
+    rng = np.random.default_rng(21)
+    B, H, Hkv, D = 2, 4, 2, 5
+    if causal:
+        N = M = 10
+        qdocs = kdocs = [(0, 4), (4, 10)]
+    else:
+        N, M = 9, 11
+        qdocs, kdocs = [(0, 3), (3, 9)], [(0, 6), (6, 11)]
+    q, k, v, d = rand_case(rng, B, H, Hkv, N, M, D, D)
+    mask = np.full((N, M), -np.inf)
+    for (n0, n1), (m0, m1) in zip(qdocs, kdocs):
+        mask[n0:n1, m0:m1] = rng.uniform(-1, 1, (n1 - n0, m1 - m0))
+    g = oracle.backward(q, k, v, d, mask, causal, 0.6)
+    for (n0, n1), (m0, m1) in zip(qdocs, kdocs):
+        r = oracle.backward(q[:, :, n0:n1], k[:, :, m0:m1], v[:, :, m0:m1], d[:, n0:n1],
+                            mask[n0:n1, m0:m1], causal, 0.6)
+        np.testing.assert_allclose(g["o"][:, n0:n1], r["o"], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(g["lse"][:, :, n0:n1], r["lse"], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(g["dq"][:, :, n0:n1], r["dq"], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(g["dk"][:, :, m0:m1], r["dk"], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(g["dv"][:, :, m0:m1], r["dv"], rtol=1e-12, atol=1e-14)
+
+
 def test_units_subset_matches_full():
     rng = np.random.default_rng(2)
     q, k, v, d = rand_case(rng, 2, 4, 2, 6, 8, 4, 4)
