@@ -1,17 +1,20 @@
 """Benchmark: attention backward TFLOP/s on GB300 through libfab's C ABI.
 
-One step = one backward over the workload, inputs resident in HBM, L2
-flushed (256 MiB write) before every step.  On the tensor-core path a step
-is fab_backward_query_pass (D_i and dQ) then fab_backward_key_pass (dK, dV),
-exactly what fab_backward enqueues, with a CUDA event between the two so
-each kernel's launch time is measured; elsewhere it is
-fab_backward_preprocess then fab_backward_main.  Throughput counts
-10*B*H*N*M*D flops per backward, halved for a causal mask.  Also reported:
-the dominant kernel's roofline against the measured dense bf16 peak, an
-end-to-end number with host buffers (pinned H2D copies of the inputs,
-fab_backward, D2H of the packed gradients), the forward kernel's TFLOP/s,
-fab_backward without o and lse (the forward recomputed inside), and the
-fp64 CPU oracle timed on a bounded sample.
+One step = one fab_backward call over the workload (what a user calls:
+on the tensor-core path the query pass, which forms D_i and dQ, then the
+key/value pass for dK and dV), inputs resident in HBM, L2 flushed (256 MiB
+write) before every step, CUDA events on the launching stream around the
+call.  Throughput counts 10*B*H*N*M*D flops per backward, halved for a
+causal mask.  A second loop, outside the timed region, calls the two passes
+through their own entry points with an event between them, which gives each
+kernel's launch time (stages_ms) and the dominant kernel's roofline against
+the measured dense bf16 peak.  Also reported: two end-to-end numbers with
+host buffers (pinned H2D copies of the inputs, fab_backward, D2H of the
+packed gradients; once with the saved o and lse, once with the op's own
+operands q, k, v, the mask and d, the forward then recomputed inside), the
+forward kernel's TFLOP/s, fab_backward without o and lse on resident inputs,
+the two-phase API's D_i kernel in GB/s, and the fp64 CPU oracle on the
+workload's (batch, key/value head) units.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl fab|reference]
 
@@ -206,22 +209,33 @@ class ClockSampler:
 
 
 def oracle_sample(w: inputs.Workload, x: dict, target_s: float = 15.0):
-    """Times the fp64 oracle on whole (batch, kv-head) units; returns (TFLOP/s, cores, sample text)."""
+    """Times the fp64 oracle, one (batch, kv-head) unit per host thread.
+
+    Every unit of the workload when that is expected to take at most
+    `target_s` on this host (about 4.5 counted GFLOP/s per core), else the
+    first units, a whole number of rounds over the cores, sized to about
+    `target_s`.  Returns (TFLOP/s, threads used, sample text, seconds)."""
     import oracle
 
     cores = os.cpu_count() or 1
     units_total = w.B * w.Hkv
-    # one unit per core, capped by the workload; shrink if one unit alone is slow
-    n_units = min(units_total, cores)
-    units = list(range(n_units))
-    t0 = time.perf_counter()
-    oracle.backward(x["q"], x["k"], x["v"], x["d"], x["mask"], w.causal, w.scale, units=units, threads=cores)
-    dt = time.perf_counter() - t0
     per_unit = backward_flops(w) / units_total
+    est_s = per_unit * units_total / (4.5e9 * cores)
+    if est_s <= target_s:
+        n_units = units_total
+    else:
+        rounds = max(1, int(target_s / (per_unit / 4.5e9)))
+        n_units = min(units_total, rounds * cores)
+    threads = min(cores, n_units)
+    units = None if n_units == units_total else list(range(n_units))
+    t0 = time.perf_counter()
+    oracle.backward(x["q"], x["k"], x["v"], x["d"], x["mask"], w.causal, w.scale, units=units, threads=threads)
+    dt = time.perf_counter() - t0
     tflops = per_unit * n_units / dt / 1e12
-    sample = (f"{n_units} of {units_total} (batch, kv-head) units of {w.name} in {dt:.1f} s; "
+    what = "all" if units is None else f"{n_units} of"
+    sample = (f"{what} {units_total} (batch, kv-head) units of {w.name} in {dt:.1f} s on {threads} threads; "
               f"counted 10*B*H*N*M*D{'/2' if w.causal else ''} flops per unit")
-    return tflops, min(cores, n_units), sample, dt
+    return tflops, threads, sample, dt
 
 
 # ----------------------------------------------------------------------------- reference arm (the oracle)
@@ -233,10 +247,9 @@ def run_reference(args, rank, world):
     w = inputs.WORKLOADS[args.workload]
     x = inputs.make(w)
     times, vals = [], []
-    cores = os.cpu_count() or 1
-    sample = ""
+    sample, c = "", 1
     for i in range(args.warmup + args.steps):
-        v, c, sample, dt = oracle_sample(w, x)
+        v, c, sample, dt = oracle_sample(w, x, target_s=6.0)
         if i >= args.warmup:
             times.append(dt)
             vals.append(v)
@@ -247,7 +260,7 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "M": w.M, "D": w.DK,
                    "causal": w.causal, "mask": w.mask, "seed": w.seed},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": min(cores, w.B * w.Hkv),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": c,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -283,7 +296,7 @@ def run_fab(args, rank, world, local):
 
     ws, packed = binding.alloc_backward(dims, dt, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    tensor_core = w.dtype == "bf16" and w.DK == w.DV and w.DK in (64, 128)
+    tensor_core = w.dtype in ("bf16", "f16") and w.DK == w.DV and w.DK in (64, 128)
 
     # fab_backward without o and lse (the op's own operands only): the forward
     # is recomputed into the workspace first; timed on its own, L2 flushed
@@ -316,7 +329,50 @@ def run_fab(args, rank, world, local):
             if i > 0:
                 pre_ms.append(e0.elapsed_time(e1))
 
-    # the two launches of one backward step (what fab_backward enqueues)
+    def step():
+        binding.fab_backward(q, k, v, d, o, lse, mask, w.causal, w.scale, ws, packed)
+
+    # kernels one fab_backward call launches: the mask scan (with a mask), the
+    # query pass and the key/value pass; on the CUDA-core path the D_i
+    # kernel, then dq_simt and dkdv_simt
+    launches_per_step = (2 + (1 if mask is not None else 0)) if tensor_core else 3
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    status = binding.fab_last_device_error()
+    if status != binding.FAB_OK:
+        raise RuntimeError(f"device error during warm-up: {binding.status_string(status)}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clk = clocks.stop()
+    status = binding.fab_last_device_error()
+    if status != binding.FAB_OK:
+        raise RuntimeError(f"device error in the timed region: {binding.status_string(status)}")
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world)
+    flops = backward_flops(w)
+    value = flops * world / (ms_max / 1e3) / 1e12
+
+    # each kernel's launch time: the same work through the two entry points
+    # fab_backward is made of, with an event between them (outside the timed
+    # region above; with a mask each entry point also scans it)
     if tensor_core:
         stage_names = ("query_pass", "key_pass")
 
@@ -334,130 +390,114 @@ def run_fab(args, rank, world, local):
         def second():
             binding.fab_backward_main(q, k, v, d, lse, mask, w.causal, w.scale, ws, packed)
 
-    def step():
-        first()
-        second()
-
-    # kernels one step launches: the query pass and the key/value pass, each
-    # entry point with a mask also scanning it (fab_backward itself scans once
-    # for both); on the CUDA-core path the D_i kernel, then dq_simt and
-    # dkdv_simt
-    launches_per_step = (2 + (2 if mask is not None else 0)) if tensor_core else 3
-
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        first()
+        second()
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     torch.cuda.synchronize()
-    status = binding.fab_last_device_error()
-    if status != binding.FAB_OK:
-        raise RuntimeError(f"device error during warm-up: {binding.status_string(status)}")
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()
-        ev[i][0].record(stream)
+        sev[i][0].record(stream)
         first()
-        ev[i][1].record(stream)
+        sev[i][1].record(stream)
         second()
-        ev[i][2].record(stream)
+        sev[i][2].record(stream)
     torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    barrier(world)
-    clk = clocks.stop()
-    status = binding.fab_last_device_error()
-    if status != binding.FAB_OK:
-        raise RuntimeError(f"device error in the timed region: {binding.status_string(status)}")
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    first_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    second_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    ms = statistics.mean(step_ms)
-    ms_max = max_over_ranks(ms, world)
-    flops = backward_flops(w)
-    value = flops * world / (ms_max / 1e3) / 1e12
+    first_ms = [e[0].elapsed_time(e[1]) for e in sev]
+    second_ms = [e[1].elapsed_time(e[2]) for e in sev]
 
     # end to end through the public call with host buffers: every step copies
     # its inputs from pinned host memory, runs fab_backward and reads the packed
-    # gradients back.  "e2e" overlaps steps (H2D of step i+1 and D2H of step
-    # i-1 run on their own streams while step i computes, two buffer sets);
-    # "serial" runs the three phases of each step back to back on one stream.
+    # gradients back.  Steps overlap (H2D of step i+1 and D2H of step i-1 run
+    # on their own streams while step i computes, two buffer sets); "serial"
+    # runs the three phases of each step back to back on one stream.  The
+    # headline copies the saved forward output and LSE with the inputs;
+    # "op_operands" copies only ggml_flash_attn_back's operands (q, k, v, the
+    # mask, d) and lets fab_backward recompute O and LSE on the device.
     e2e = None
     if not args.no_e2e:
         host = {kk: vv.pin_memory() for kk, vv in xc.items() if isinstance(vv, torch.Tensor)}
         host["o"] = o.cpu().pin_memory()
         host["lse"] = lse.cpu().pin_memory()
-        names = [n for n in ("q", "k", "v", "d", "mask", "o", "lse") if n in host]
-        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
         d2h = packed.numel() * 4
-        sets = []
-        for _ in range(2):
-            bufs = {n: torch.empty_like(host[n], device=dev) for n in names}
-            wsb, pkb = binding.alloc_backward(dims, dt, dev)
-            sets.append((bufs, wsb, pkb, torch.empty(packed.numel(), dtype=torch.float32).pin_memory()))
         s_h2d, s_cmp, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-        def run_pipelined(nsteps):
-            ev_in = [torch.cuda.Event() for _ in range(2)]
-            ev_cmp = [torch.cuda.Event() for _ in range(2)]
-            ev_out = [torch.cuda.Event() for _ in range(2)]
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0.record(s_h2d)
-            for i in range(nsteps):
-                bufs, wsb, pkb, outh = sets[i % 2]
-                if i >= 2:
-                    s_h2d.wait_event(ev_cmp[i % 2])  # inputs of step i-2 consumed
-                with torch.cuda.stream(s_h2d):
+        def e2e_variant(saved: bool):
+            names = [n for n in ("q", "k", "v", "d", "mask") + (("o", "lse") if saved else ()) if n in host]
+            h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+            sets = []
+            for _ in range(2):
+                bufs = {n: torch.empty_like(host[n], device=dev) for n in names}
+                wsb, pkb = binding.alloc_backward(dims, dt, dev, recompute=not saved)
+                sets.append((bufs, wsb, pkb, torch.empty(packed.numel(), dtype=torch.float32).pin_memory()))
+
+            def call(bufs, wsb, pkb, strm):
+                binding.fab_backward(bufs["q"], bufs["k"], bufs["v"], bufs["d"], bufs.get("o"), bufs.get("lse"),
+                                     bufs.get("mask"), w.causal, w.scale, wsb, pkb, stream=strm)
+
+            def run_pipelined(nsteps):
+                ev_in = [torch.cuda.Event() for _ in range(2)]
+                ev_cmp = [torch.cuda.Event() for _ in range(2)]
+                ev_out = [torch.cuda.Event() for _ in range(2)]
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(s_h2d)
+                for i in range(nsteps):
+                    bufs, wsb, pkb, outh = sets[i % 2]
+                    if i >= 2:
+                        s_h2d.wait_event(ev_cmp[i % 2])  # inputs of step i-2 consumed
+                    with torch.cuda.stream(s_h2d):
+                        for n in names:
+                            bufs[n].copy_(host[n], non_blocking=True)
+                        ev_in[i % 2].record(s_h2d)
+                    s_cmp.wait_event(ev_in[i % 2])
+                    if i >= 2:
+                        s_cmp.wait_event(ev_out[i % 2])  # packed of step i-2 read back
+                    call(bufs, wsb, pkb, s_cmp)
+                    ev_cmp[i % 2].record(s_cmp)
+                    s_d2h.wait_event(ev_cmp[i % 2])
+                    with torch.cuda.stream(s_d2h):
+                        outh.copy_(pkb, non_blocking=True)
+                        ev_out[i % 2].record(s_d2h)
+                s_d2h.wait_event(ev_out[(nsteps - 1) % 2])
+                t1.record(s_d2h)
+                t1.synchronize()
+                return t0.elapsed_time(t1) / nsteps
+
+            def run_serial(nsteps):
+                bufs, wsb, pkb, outh = sets[0]
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(stream)
+                for _ in range(nsteps):
                     for n in names:
                         bufs[n].copy_(host[n], non_blocking=True)
-                    ev_in[i % 2].record(s_h2d)
-                s_cmp.wait_event(ev_in[i % 2])
-                if i >= 2:
-                    s_cmp.wait_event(ev_out[i % 2])  # packed of step i-2 read back
-                binding.fab_backward(bufs["q"], bufs["k"], bufs["v"], bufs["d"], bufs["o"], bufs["lse"],
-                                     bufs.get("mask"), w.causal, w.scale, wsb, pkb, stream=s_cmp)
-                ev_cmp[i % 2].record(s_cmp)
-                s_d2h.wait_event(ev_cmp[i % 2])
-                with torch.cuda.stream(s_d2h):
+                    call(bufs, wsb, pkb, stream)
                     outh.copy_(pkb, non_blocking=True)
-                    ev_out[i % 2].record(s_d2h)
-            s_d2h.wait_event(ev_out[(nsteps - 1) % 2])
-            t1.record(s_d2h)
-            t1.synchronize()
-            return t0.elapsed_time(t1) / nsteps
+                t1.record(stream)
+                t1.synchronize()
+                return t0.elapsed_time(t1) / nsteps
 
-        def run_serial(nsteps):
-            bufs, wsb, pkb, outh = sets[0]
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0.record(stream)
-            for _ in range(nsteps):
-                for n in names:
-                    bufs[n].copy_(host[n], non_blocking=True)
-                binding.fab_backward(bufs["q"], bufs["k"], bufs["v"], bufs["d"], bufs["o"], bufs["lse"],
-                                     bufs.get("mask"), w.causal, w.scale, wsb, pkb)
-                outh.copy_(pkb, non_blocking=True)
-            t1.record(stream)
-            t1.synchronize()
-            return t0.elapsed_time(t1) / nsteps
+            run_pipelined(max(2, args.warmup))
+            run_serial(max(1, args.warmup))
+            torch.cuda.synchronize()
+            barrier(world)
+            pipe_ms = max_over_ranks(run_pipelined(args.steps), world)
+            barrier(world)
+            ser_ms = max_over_ranks(run_serial(args.steps), world)
+            status = binding.fab_last_device_error()
+            if status != binding.FAB_OK:
+                raise RuntimeError(f"device error in the e2e region: {binding.status_string(status)}")
+            del sets
+            return {"value": round(flops * world / (pipe_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+                    "ms_per_step": round(pipe_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "serial": {"value": round(flops * world / (ser_ms / 1e3) / 1e12, 3),
+                               "ms_per_step": round(ser_ms, 3)}}
 
-        run_pipelined(max(2, args.warmup))
-        run_serial(max(1, args.warmup))
-        torch.cuda.synchronize()
-        barrier(world)
-        pipe_ms = max_over_ranks(run_pipelined(args.steps), world)
-        barrier(world)
-        ser_ms = max_over_ranks(run_serial(args.steps), world)
-        e2e = {"value": round(flops * world / (pipe_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
-               "ms_per_step": round(pipe_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "mode": "two buffer sets, H2D / backward / D2H on three streams, steps overlapped",
-               "serial": {"value": round(flops * world / (ser_ms / 1e3) / 1e12, 3), "ms_per_step": round(ser_ms, 3)}}
-        status = binding.fab_last_device_error()
-        if status != binding.FAB_OK:
-            raise RuntimeError(f"device error in the e2e region: {binding.status_string(status)}")
+        e2e = e2e_variant(True)
+        e2e["mode"] = "two buffer sets, H2D / backward / D2H on three streams, steps overlapped; o and lse copied in"
+        e2e["op_operands"] = e2e_variant(False)
+        e2e["op_operands"]["mode"] = ("as above, copying q, k, v, the mask and d only; fab_backward with o = lse = "
+                                      "NULL recomputes the forward on the device (backward flops counted)")
 
     peaks, peak_src = load_peaks()
     first_mean, second_mean = statistics.mean(first_ms), statistics.mean(second_ms)
@@ -479,7 +519,8 @@ def run_fab(args, rank, world, local):
                 "traffic": args.traffic_bytes if args.traffic_bytes is not None else MEASURED_TRAFFIC.get((w.name, kkey)),
                 "kernel": kname, "kernel_ms": round(kms, 4), "kernel_flops": kflops,
                 "tiles_run": round(frac_run, 4),
-                "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone between L2 flushes)"}
+                "peak_source": (f"{peak_src} bf16_tflops (burst: the kernel is timed alone between L2 flushes)"
+                                + ("; f16 has the same nominal dense rate as bf16 (ratio 1)" if w.dtype == "f16" else ""))}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -490,17 +531,19 @@ def run_fab(args, rank, world, local):
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "M": w.M, "D": w.DK,
                        "causal": w.causal, "mask": w.mask, "seed": w.seed, "parallelism": f"replicas x{world}",
-                       "l2": "flushed before every step (256 MiB write)"},
+                       "l2": "flushed before every step (256 MiB write)",
+                       "timed": "one fab_backward call per step (CUDA events on its stream)"},
             "frac_of_peak": round(value / world / peak, 4),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
-            "stages_ms": {stage_names[0]: round(first_mean, 4), stage_names[1]: round(second_mean, 4)},
+            "stages_ms": {stage_names[0]: round(first_mean, 4), stage_names[1]: round(second_mean, 4),
+                          "note": "each entry point timed on its own, outside the timed region"},
             "wall_s": round(wall, 4),
             "forward": ({"tflops": round(forward_flops(w) / (statistics.median(fwd_ms) / 1e3) / 1e12, 2),
                          "ms": round(statistics.median(fwd_ms), 3),
