@@ -2,10 +2,10 @@
 
 Small cases span several key/query tiles, ragged tails, GQA, batches, causal
 and additive masks, D = 64 and 128 on the tensor-core path and odd widths /
-f32 on the CUDA-core path.  The five measured workloads run at full size in
-the launch configuration the benchmark times; where the oracle would take
-minutes, it computes a sample of (batch, key/value head) units exactly and
-the comparison covers those units.
+f32 on the CUDA-core path.  The five measured workloads (and the two extra
+masked ones) run at full size in the launch configuration the benchmark
+times, and every element of dQ, dK, dV, O and LSE is compared with the
+oracle's.
 """
 import zlib
 
@@ -144,29 +144,20 @@ def test_repeat_calls_identical():
 
 # ----------------------------------------------------------------------------- the five workloads
 
-# (units, rows) the oracle computes exactly at full size; None = everything
-FULL_SAMPLE = {
-    "tiny_f32": (None, None),
-    "causal_d64": (None, None),
-    "gqa_causal_d128": ([0, 13, 31], None),
-    "long_seq": ([5], (16384 - 1024, 16384)),
-    "masked_nonsquare": ([0, 9, 30], None),
-    "padded_d128": ([0, 13, 31], None),
-    "docs_d128": ([0, 13, 31], None),
-}
-
-
 @pytest.mark.parametrize("name", inputs.ORDER + inputs.EXTRA)
 def test_workload_parity(name):
     w = inputs.WORKLOADS[name]
     x = inputs.make(w)
     gpu = run_gpu(w, x)
-    units, rows = FULL_SAMPLE[name]
-    ref = oracle_ref(w, x, units=units, rows=rows)
-    errs = compare(w, gpu, ref, units=units, rows=rows)
+    # every unit and every row: the oracle runs one (batch, key/value head)
+    # unit per host thread (long_seq: 16 units of one 16384-row head each)
+    ref = oracle_ref(w, x)
+    errs = compare(w, gpu, ref)
     tol = TOL[w.dtype]
     for key in ("dq", "dk", "dv", "o"):
         assert errs[key] <= tol, (name, key, errs)
+    fin = np.isfinite(ref["lse"])
+    assert errs["lse"] <= 1e-3 * max(1.0, float(np.max(np.abs(ref["lse"][fin])))), errs
     check_pads_zero(w, gpu["packed"])
     assert np.all(np.isfinite(gpu["packed"]))
     if w.mask == "random":
