@@ -59,7 +59,7 @@ bool forward_tc_supported(const Problem& p);
 cudaError_t launch_forward_tc(const Problem& p, void* o, float* lse, cudaStream_t s);
 
 // fab_bwd_tc.cu: the tcgen05 tensor-core backward's key/value pass (dK, dV;
-// bf16, DK == DV in {64, 128}).
+// bf16 or f16, DK == DV in {64, 128}).
 bool backward_tc_supported(const Problem& p);
 cudaError_t launch_backward_tc(const Problem& p, cudaStream_t s);
 

@@ -13,7 +13,10 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it (FAB_NOALLOC_MAX_ROWS floats, 4 MiB) until the process
 // exits.  Its device address is looked up once per device, with that device
-// current, on the first call there.  All calls on a device share the array:
+// current, on the first call there, and kept for the rest of the process: a
+// cudaDeviceReset (or any other teardown of the device's primary context)
+// would leave that address stale, so the entry point must not be called on
+// that device again afterwards.  All calls on a device share the array:
 // two calls whose work overlaps on the GPU (different streams, no ordering
 // between them) race on it.  Nothing in it has to start at zero: each call
 // overwrites every D_i entry and map byte it reads before reading it.  When

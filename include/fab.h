@@ -142,7 +142,7 @@ FAB_EXPORT int fab_forward_lse(const void* q, const void* k, const void* v, cons
  * workspace: device, >= fab_backward_workspace_bytes() bytes (with o and lse
  * NULL: fab_backward_recompute_workspace_bytes()), contents overwritten.  packed_out: device f32, fab_packed_bytes() bytes, fully
  * overwritten (padding written as 0).  Where the tensor-core kernels apply
- * (bf16, DK == DV in {64, 128}) it enqueues fab_backward_query_pass then
+ * (bf16 or f16, DK == DV in {64, 128}) it enqueues fab_backward_query_pass then
  * fab_backward_key_pass; otherwise fab_backward_preprocess then
  * fab_backward_main. */
 FAB_EXPORT int fab_backward(const void* q, const void* k, const void* v, const void* d, const void* o, const float* lse,
@@ -162,8 +162,8 @@ FAB_EXPORT int fab_backward_main(const void* q, const void* k, const void* v, co
                       const uint16_t* mask, int causal, float scale, int dtype, const fab_dims* dims,
                       const void* workspace, size_t workspace_bytes, float* packed_out, fab_stream stream);
 
-/* The two tensor-core passes that make up fab_backward for bf16 inputs with
- * DK == DV in {64, 128} (labml "Backward pass"); FAB_ERR_UNSUPPORTED
+/* The two tensor-core passes that make up fab_backward for bf16 or f16 inputs
+ * with DK == DV in {64, 128} (labml "Backward pass"); FAB_ERR_UNSUPPORTED
  * otherwise.  Same arguments as fab_backward.
  * fab_backward_query_pass: D_i = dO_i . O_i into the workspace, the dQ slice
  * of packed_out (dQ_n = scale sum_m dS_nm K_m, recomputing S and dP per query
@@ -195,7 +195,8 @@ FAB_EXPORT int fab_backward_key_pass(const void* q, const void* k, const void* v
  * FAB_ERR_WORKSPACE when B*H*N exceeds FAB_NOALLOC_MAX_ROWS; allocates and
  * frees nothing.  The first call on a device looks up the array's device
  * address with that device current; make that first call before any stream
- * capture.  Calls on one device share the array, so two calls that may run
+ * capture.  The address is kept for the life of the process: after a
+ * cudaDeviceReset of that device, do not call this entry point there again.  Calls on one device share the array, so two calls that may run
  * at the same time on the GPU (on unordered streams) race; order them.  No
  * part of the array needs clearing between calls. */
 FAB_EXPORT int fab_backward_noalloc(const void* q, const void* k, const void* v, const void* d, const void* o,

@@ -57,14 +57,25 @@ def test_noalloc_matches_fab_backward_on_consecutive_calls(w):
         assert np.all(got[nq:off_k] == 0) and np.all(got[off_k + nk:off_v] == 0) and np.all(got[off_v + nv:] == 0)
 
 
-def test_noalloc_rejects_rows_beyond_the_scratch():
-    # B*H*N one past the limit: refused on the host before anything is launched
-    n = binding.NOALLOC_MAX_ROWS // 8 + 1
-    dims = binding.make_dims(1, 8, 8, n, 64, 64, 64)
-    import ctypes
-
-    fake = 0x10000
-    vp = ctypes.c_void_p
-    rc = binding.lib().fab_backward_noalloc(vp(fake), vp(fake), vp(fake), vp(fake), vp(fake), vp(fake), None, 0,
-                                            1.0, binding.FAB_BF16, ctypes.byref(dims), vp(fake), None)
-    assert rc == binding.FAB_ERR_WORKSPACE
+def test_noalloc_at_the_row_limit_with_a_mask():
+    # B*H*N exactly FAB_NOALLOC_MAX_ROWS: D_i fills the whole fixed array, so
+    # the mask's live-tile maps do not fit after it and the call computes
+    # every tile; fab_backward on a caller workspace that holds the maps skips
+    # the all -inf tiles.  A skipped tile only ever adds +0, so the two must
+    # agree bit for bit, on two calls in a row.
+    w = inputs.custom(1, 64, 8, binding.NOALLOC_MAX_ROWS // 64, 128, 64, mask="pad", mask_p=0.05, seed=45,
+                      name="row_limit_masked")
+    assert w.B * w.H * w.N == binding.NOALLOC_MAX_ROWS
+    x = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inputs.make(w).items()}
+    o, lse = binding.forward(x["q"], x["k"], x["v"], x["mask"], w.causal, w.scale)
+    dims = binding.dims_of(x["q"], x["k"], x["v"])
+    ws, want = binding.alloc_backward(dims, binding.dtype_code(x["q"]), x["q"].device)
+    binding.fab_backward(x["q"], x["k"], x["v"], x["d"], o, lse, x["mask"], w.causal, w.scale, ws, want)
+    assert binding.fab_last_device_error() == binding.FAB_OK
+    assert torch.isfinite(want).all()
+    out = torch.empty_like(want)
+    for call in range(2):
+        out.fill_(float("nan"))
+        binding.fab_backward_noalloc(x["q"], x["k"], x["v"], x["d"], o, lse, x["mask"], w.causal, w.scale, out)
+        assert binding.fab_last_device_error() == binding.FAB_OK
+        assert torch.equal(out, want), call
