@@ -53,12 +53,19 @@
 // one to two hundred cycles at every commit and barrier wait; with two
 // streams those stalls overlap the other stream's MMAs.
 //
+// Unit switch: a unit's key and value tiles are released as soon as its last
+// S^T and dP^T finish, so the next unit's are loaded while the unit's last
+// dV/dK products and its epilogue run.  The softmax warps write dV and dK
+// themselves (through shared memory, whole rows to global memory), which
+// leaves the TMA unit to the loads: bulk tensor stores of the 128 KB ahead
+// of the next key tile held that load back by some 3,000 cycles.
+//
 // Warps (352 threads): 0 = TMA producer (and the tile's LSE and D rows);
-// 1 = tensor-memory allocator and S^T/dP^T issuer; 10 = dV/dK issuer and the
-// epilogue's bulk stores (lane 0 of an issuer warp issues); 2-9 = softmax/dS
-// and the epilogue staging (thread = key row; two warps per tensor-memory
-// lane quarter, each taking 64 of the tile's 128 queries).  All hand-offs are mbarriers; every wait is bounded
-// (see fab_device.cuh).
+// 1 = tensor-memory allocator and S^T/dP^T issuer; 10 = dV/dK issuer (lane 0
+// of an issuer warp issues); 2-9 = softmax/dS and the epilogue (thread = key
+// row; two warps per tensor-memory lane quarter, each taking 64 of the tile's
+// 128 queries).  All hand-offs are mbarriers; every wait is bounded (see
+// fab_device.cuh).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -106,10 +113,9 @@ struct Cfg {
   static constexpr uint32_t ID_DVK = idesc_16(128, D, false, true, F16);
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(TM_DK + D <= TM_COLS, "tensor memory budget");
-  // epilogue staging (f32, 32-column atoms): dV over the key and value
-  // tiles, dK over one Q and one dO stage
-  static_assert((D / 32) * ATOM == OFF_V + TILE - OFF_K, "dV staging fills the key/value tiles");
-  static_assert((D / 64) * ATOM == TILE, "each half of dK fills one ring stage");
+  // epilogue staging: one slot of 32 key rows x D/2 f32 columns per softmax
+  // warp, four to a Q or dO stage
+  static_assert(4 * 32 * (D / 2) * 4 == TILE, "four epilogue slots fill one ring stage");
   static_assert(QST <= 4 && OST <= QST, "barrier slots hold up to four stages; the dO ring is not deeper");
 };
 
@@ -127,7 +133,7 @@ enum : int {
   B_FIN_S = 22,   // every S^T and dP^T MMA finished
   B_FIN_X = 23,   // every dV/dK MMA finished
   B_DF = 24,      // phase k: unit k's epilogue read dV, dK from tensor memory
-  B_STG = 25,     // phase k: unit k's dV, dK are staged in shared memory
+  B_KVF = 25,     // phase k: unit k's S^T and dP^T MMAs finished (its key and value tiles are free)
   B_V = 26,       // phase k: unit k's value tile landed
   B_COUNT = 27
 };
@@ -149,7 +155,6 @@ template <int D, bool MASK, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                   const Params p) {
   using C = Cfg<D, F16>;
   extern __shared__ uint8_t smem_raw[];
@@ -163,11 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 4);
-  // units whose dV/dK staging the bulk stores have finished reading: the
-  // part in the key tile, the part in the value tile, the part in one Q and
-  // one dO stage (in that order)
-  uint32_t* k_cnt = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 8);
-  uint32_t* v_cnt = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 12);
+  // epilogue slots released: one count per softmax warp per unit
   uint32_t* r_cnt = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 16);
   float* ld_smem = reinterpret_cast<float*>(smem + C::OFF_LD);
   uint32_t* err = &g_err_tc;
@@ -241,8 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
-    *k_cnt = 0u;
-    *v_cnt = 0u;
     *r_cnt = 0u;
     mbar_init(bar(B_KV), 1);
     mbar_init(bar(B_V), 1);
@@ -261,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_FIN_S), 1);
     mbar_init(bar(B_FIN_X), 1);
     mbar_init(bar(B_DF), kSoftmaxThreads);
-    mbar_init(bar(B_STG), kSoftmaxThreads);
+    mbar_init(bar(B_KVF), 1);
     fence_mbar_init();
     // this thread is the producer's issuing lane: start the first unit's
     // key/value tile copies before the tensor-memory allocation and block
@@ -296,11 +295,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     // Per unit: an L2 prefetch of the next unit's key/value tiles, Q_g and
     // dO_g (with the tile's LSE and D rows) for every tile g, the key/value
-    // tiles after the first tile's.  Stages and barrier phases count tiles g
-    // across units.  A unit's epilogue stages dV in the key and value tiles
-    // and dK in the Q and dO stages of its last tile G, so the next unit's
-    // key tile, value tile, Q_{G+QST} and dO_{G+OST} also wait for that
-    // unit's bulk stores to have read the part they overwrite.
+    // tiles after the first tile's, as soon as the previous unit's last S^T
+    // and dP^T are done with theirs.  Stages and barrier phases count tiles g
+    // across units.  A unit's epilogue passes dV and dK through the Q and dO
+    // stages of its last tile G, so Q_{G+QST} and dO_{G+OST} also wait for
+    // the softmax warps to have released them.
     int g = 0, ku = 0, q_issued = 0, o_issued = 0;
     int kv_issued = 0;  // the first unit's copies were started at barrier initialisation
     for (int kk = 0; kv_issued == 0 && unit_at(kk) < n_units; ++kk)
@@ -312,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto staged_wait = [&](int gg, int dist) {
 #pragma unroll
       for (int i = 0; i < 3; ++i)
-        if (stG[i] + dist == gg) return counter_wait(r_cnt, (uint32_t)(stK[i] + 1), abort_flag, err);
+        if (stG[i] + dist == gg)
+          return counter_wait(r_cnt, (uint32_t)(kSoftmaxThreads / 32) * (uint32_t)(stK[i] + 1), abort_flag, err);
       return true;
     };
     for (int kk = 0; ok && unit_at(kk) < n_units; ++kk) {
@@ -375,30 +375,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one arrival per lane (count 32) publishes that lane's LSE/D stores
         mbar_arrive(bar(B_FO + os));
         ++o_issued;
-        if (it == 0) {
-          // the unit's key and value tiles (the first unit's were started
-          // at barrier initialisation): the previous unit's dV staging there
-          // must have been read
-          if (ku > 0) {
-            const int kvrow = x.b * (int)p.Hkv + x.hkv;
-            ok = counter_wait(k_cnt, (uint32_t)ku, abort_flag, err);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            fence_proxy_async_smem();
-            if (lane == 0) {
-              mbar_arrive_expect_tx(bar(B_KV), C::TILE);
-              for (int a = 0; a < C::ATOMS; ++a)
-                tma_load_3d(sbase + C::OFF_K + a * C::ATOM, &tmK, bar(B_KV), a * 64, x.m0, kvrow);
+        if (it == 0 && ku > 0) {
+          // the unit's key and value tiles (the first unit's were started at
+          // barrier initialisation), once the previous unit's last S^T and
+          // dP^T products are done with theirs
+          const int kvrow = x.b * (int)p.Hkv + x.hkv;
+          ok = mbar_wait(bar(B_KVF), (ku - 1) & 1, abort_flag, err);
+          if (!__all_sync(0xffffffffu, ok)) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B_KV), C::TILE);
+            mbar_arrive_expect_tx(bar(B_V), C::TILE);
+            for (int a = 0; a < C::ATOMS; ++a) {
+              tma_load_3d(sbase + C::OFF_K + a * C::ATOM, &tmK, bar(B_KV), a * 64, x.m0, kvrow);
+              tma_load_3d(sbase + C::OFF_V + a * C::ATOM, &tmV, bar(B_V), a * 64, x.m0, kvrow);
             }
-            ok = counter_wait(v_cnt, (uint32_t)ku, abort_flag, err);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            fence_proxy_async_smem();
-            if (lane == 0) {
-              mbar_arrive_expect_tx(bar(B_V), C::TILE);
-              for (int a = 0; a < C::ATOMS; ++a)
-                tma_load_3d(sbase + C::OFF_V + a * C::ATOM, &tmV, bar(B_V), a * 64, x.m0, kvrow);
-            }
-            ++kv_issued;
           }
+          ++kv_issued;
         }
       }
       stG[ku % 3] = g - 1;
@@ -471,6 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(g + 1);
           }
         }
+        // the unit's key and value tiles are free once these products finish
+        mma_commit(bar(B_KVF), issue);
         ++ku;
       }
       mma_commit(bar(B_FIN_S), issue);
@@ -479,8 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dV += P^T dO_g and dK += dS^T Q_g once the softmax warps wrote
       // P^T(g), dS^T(g) into X: packed 16-bit, queries 32 c .. 32 c + 31 at
       // columns 32 c + 0..15 (P) and 32 c + 16..31 (dS).  A unit's first
-      // products wait for the previous unit's epilogue to have read dV, dK;
-      // after its last, this warp writes the staged dV, dK out.
+      // products wait for the previous unit's epilogue to have read dV, dK.
       const uint64_t dO_mn = sdesc_sw128(sbase + C::OFF_DO, C::ATOM, 1024);  // stage 0, MN-major
       const uint64_t dQ_mn = sdesc_sw128(sbase + C::OFF_Q, C::ATOM, 1024);
       auto p_col = [](int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); };
@@ -507,36 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MMA of the unit) are complete for the epilogue
         mma_commit(bar(B_FINAL), issue);
         if (!ok) break;
-        // once the softmax warps staged dV, dK: write them out, and release
-        // the staging once the stores have read it
-        if (!(ok = wall(B_STG, ku & 1))) break;
-        if (lane == 0) {
-          // three groups: dV's first half (key tile), its second (value
-          // tile), dK (ring stages), each released once the stores read it
-          const int G = g - 1;
-          const int kvrow = x.b * (int)p.Hkv + x.hkv;
-          for (int a = 0; a < D / 32; ++a) {
-            tma_store_3d(&tmDV, sbase + C::OFF_K + a * C::ATOM, a * 32, x.m0, kvrow);
-            if (a + 1 == D / 64 || a + 1 == D / 32) bulk_commit_group();
-          }
-          for (int a = 0; a < D / 32; ++a) {
-            const uint32_t src = a < D / 64 ? sbase + C::OFF_Q + (uint32_t)(G % C::QST) * C::TILE + a * C::ATOM
-                                            : sbase + C::OFF_DO + (uint32_t)(G % C::OST) * C::TILE +
-                                                  (a - D / 64) * C::ATOM;
-            tma_store_3d(&tmDK, src, a * 32, x.m0, kvrow);
-          }
-          bulk_commit_group();
-          bulk_wait_read_2();
-          counter_bump(k_cnt);
-          bulk_wait_read_1();
-          counter_bump(v_cnt);
-          bulk_wait_read_all();
-          counter_bump(r_cnt);
-        }
-        __syncwarp();
         ++ku;
       }
-      if (lane == 0) bulk_wait_read_all();  // (every group was waited for above; kept for an early exit)
       mma_commit(bar(B_FIN_X), issue);
       mbar_drain(bar(B_FIN_X), 0);
     }
@@ -685,47 +650,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // epilogue: dV and dK (scaled) of this key tile, half of the columns
-      // per warp, as 32-column atoms of 128-byte swizzled rows: dV in the
-      // key/value tiles, dK's first D/2 columns in the Q stage of the unit's
-      // last tile G, the rest in its dO stage (every product reading them is
-      // done; the producer holds the next loads into them until the stores
-      // have read them).  The dV/dK issuer writes them out (rows past M are
-      // clipped by the store).  The tensor-memory loads are warp
-      // collectives, so every lane runs them.
+      // epilogue: dV and dK (scaled) of this key tile.  Each warp writes its
+      // 32 key rows x D/2 columns, dV first, then dK, through its own slot in
+      // the Q stage (warps 2-5) or the dO stage (warps 6-9) of the unit's
+      // last tile G (every product reading them is done): tensor memory ->
+      // registers -> the slot, a row per thread, its 16-byte chunks rotated
+      // by the row so that neither these writes nor the column-wise reads
+      // below conflict on banks -> global memory, each 16 lanes one half row
+      // of whole 128-byte lines.  Rows past M are skipped.  The producer
+      // holds the next loads into those stages until every warp has
+      // released its slot; the key and value tiles were released when the
+      // unit's last S^T and dP^T finished, so the next unit's are on their
+      // way.  The tensor-memory loads are warp collectives, so every lane
+      // runs them.
       const int G = g - 1;
       const bool done = mbar_wait(bar(B_FINAL), ku & 1, abort_flag, err);
       const bool write = __all_sync(0xffffffffu, done && !*abort_flag);
       if (!write) break;
       tc_fence_after();
+      constexpr int CH = D / 8;      // 16-byte chunks in a slot row (D/2 f32)
+      constexpr int ROWB = CH * 16;  // slot row bytes
+      constexpr int RPI = 32 / CH;   // slot rows per read instruction
+      const uint32_t slot = (hf == 0 ? sbase + C::OFF_Q + (uint32_t)(G % C::QST) * C::TILE
+                                     : sbase + C::OFF_DO + (uint32_t)(G % C::OST) * C::TILE) +
+                            (uint32_t)(warp & 3) * (32u * ROWB);
+      const int mw = x.m0 + (warp & 3) * 32;  // this warp's first key
+      const int64_t kvrow0 = ((int64_t)x.b * p.Hkv + x.hkv) * p.M;
+      auto stage = [&](uint32_t tcol, float mul) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
-        uint32_t rv[32], rk[32];
-        tmem_ld32(tm + lane_off + C::TM_DV + hf * (D / 2) + c0, rv);
-        tmem_ld32(tm + lane_off + C::TM_DK + hf * (D / 2) + c0, rk);
-        tmem_ld_wait2(rv, rk);
-        const int a = (hf * (D / 2) + c0) / 32;  // atom (32 columns)
-        const uint32_t rowv = sbase + C::OFF_K + (uint32_t)a * C::ATOM + r * 128;
-        const uint32_t rowk = (a < D / 64 ? sbase + C::OFF_Q + (uint32_t)(G % C::QST) * C::TILE + (uint32_t)a * C::ATOM
-                                          : sbase + C::OFF_DO + (uint32_t)(G % C::OST) * C::TILE +
-                                                (uint32_t)(a - D / 64) * C::ATOM) +
-                              r * 128;
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t rv[32];
+          tmem_ld32(tm + lane_off + tcol + hf * (D / 2) + c0, rv);
+          tmem_ld_wait(rv);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k ^ (r & 7)) << 4;
-          st_shared_v4(rowv + off, rv[4 * k], rv[4 * k + 1], rv[4 * k + 2], rv[4 * k + 3]);
-          st_shared_v4(rowk + off, __float_as_uint(p.scale * __uint_as_float(rk[4 * k])),
-                       __float_as_uint(p.scale * __uint_as_float(rk[4 * k + 1])),
-                       __float_as_uint(p.scale * __uint_as_float(rk[4 * k + 2])),
-                       __float_as_uint(p.scale * __uint_as_float(rk[4 * k + 3])));
+          for (int k = 0; k < 8; ++k) {
+            const int c = c0 / 4 + k;
+            st_shared_v4(slot + (uint32_t)lane * ROWB + ((uint32_t)(c ^ (lane & 7)) << 4),
+                         __float_as_uint(mul * __uint_as_float(rv[4 * k])),
+                         __float_as_uint(mul * __uint_as_float(rv[4 * k + 1])),
+                         __float_as_uint(mul * __uint_as_float(rv[4 * k + 2])),
+                         __float_as_uint(mul * __uint_as_float(rv[4 * k + 3])));
+          }
         }
-      }
-      fence_proxy_async_smem();
-      // dV, dK have been read: the next unit's first products may overwrite
-      // them; and they are staged: the dV/dK issuer writes them out
+        __syncwarp();
+      };
+      auto drain = [&](float* dst) {
+#pragma unroll 4
+        for (int i = 0; i < CH; ++i) {
+          const int rr = i * RPI + lane / CH, cl = lane % CH;
+          const uint4 v = ld_shared_v4(slot + (uint32_t)rr * ROWB + ((uint32_t)(cl ^ (rr & 7)) << 4));
+          if (mw + rr < p.M)
+            __stcs(reinterpret_cast<float4*>(dst + (kvrow0 + mw + rr) * D + hf * (D / 2) + cl * 4),
+                   make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                               __uint_as_float(v.w)));
+        }
+        __syncwarp();
+      };
+      stage(C::TM_DV, 1.f);
+      drain(p.dv);
+      stage(C::TM_DK, p.scale);
+      // dV, dK have been read: the next unit's first products may overwrite them
       tc_fence_before();
       mbar_arrive(bar(B_DF));
-      mbar_arrive(bar(B_STG));
+      drain(p.dk);
+      if (lane == 0) counter_bump(r_cnt);
       ++ku;
     }
   }
@@ -753,7 +741,7 @@ template <int D, bool MASK, bool F16>
 cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   using C = Cfg<D, F16>;
   const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUtensorMap mq, mk, mv, mo, mdk, mdv;
+  CUtensorMap mq, mk, mv, mo;
   const cuuint64_t e = 2;  // bytes per 16-bit element
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.N, (cuuint64_t)(pr.H * pr.B)};
@@ -774,15 +762,6 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
     const cuuint64_t str[3] = {D * e, (cuuint64_t)pr.H * D * e, (cuuint64_t)pr.N * pr.H * D * e};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)C::BQ, 1};
     if (!make_map(&mo, pr.d, 4, dims, str, box, dt)) return cudaErrorInvalidValue;
-  }
-  {
-    // the packed f32 dK and dV slices [D,M,Hkv,B], stored in 32-column (128-byte) boxes
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)pr.M, (cuuint64_t)(pr.Hkv * pr.B)};
-    const cuuint64_t str[2] = {D * 4, (cuuint64_t)pr.M * D * 4};
-    const cuuint32_t box[3] = {32, (cuuint32_t)C::BM, 1};
-    const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    if (!make_map(&mdk, pr.packed + pr.off_k / 4, 3, dims, str, box, f32)) return cudaErrorInvalidValue;
-    if (!make_map(&mdv, pr.packed + pr.off_v / 4, 3, dims, str, box, f32)) return cudaErrorInvalidValue;
   }
   Params p;
   p.B = pr.B;
@@ -807,7 +786,7 @@ cudaError_t launch_d(const Problem& pr, cudaStream_t s) {
   cudaError_t err =
       cudaFuncSetAttribute(bwd_tc_kernel<D, MASK, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  bwd_tc_kernel<D, MASK, F16><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, mdk, mdv, p);
+  bwd_tc_kernel<D, MASK, F16><<<(unsigned)grid, kThreads, C::SMEM, s>>>(mq, mk, mv, mo, p);
   return cudaPeekAtLastError();
 }
 

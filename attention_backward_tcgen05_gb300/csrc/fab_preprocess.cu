@@ -151,8 +151,19 @@ cudaError_t launch_preprocess(const Problem& p, cudaStream_t s) {
     lpr = 1;
     while (lpr < 32 && lpr < chunks) lpr <<= 1;
   }
+  // one wave: as many blocks as the SMs hold at once (a grid of 1.6 waves
+  // left the last 0.6 of them running alone), fewer for a small problem
+  int per_sm = 0;
+  cudaError_t oe;
+  if (p.dtype == FAB_BF16)
+    oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, preprocess_kernel<__nv_bfloat16>, 256, 0);
+  else if (p.dtype == FAB_F16)
+    oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, preprocess_kernel<__half>, 256, 0);
+  else
+    oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, preprocess_kernel<float>, 256, 0);
+  if (oe != cudaSuccess || per_sm < 1) per_sm = 1;
   int64_t blocks = (rows * lpr / 32 + 7) / 8 + 1;
-  const int64_t cap = (int64_t)sms * 8;
+  const int64_t cap = (int64_t)sms * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (p.dtype == FAB_BF16) {
