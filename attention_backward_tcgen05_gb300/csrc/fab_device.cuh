@@ -162,8 +162,6 @@ FAB_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 
 // As bulk_wait_read_all, but only for all but the most recent group.
 FAB_DEV void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
-// As bulk_wait_read_all, but only for all but the two most recent groups.
-FAB_DEV void bulk_wait_read_2() { asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); }
 
 // Tiled bulk prefetch global -> L2 (no destination, no completion): warms L2
 // for a later tma_load_3d of the same box.
@@ -173,10 +171,6 @@ FAB_DEV void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
                "r"(c0), "r"(c1), "r"(c2)
                : "memory");
 }
-
-// Waits until every bulk store this thread committed has completed (global
-// writes done, shared memory free).
-FAB_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Barrier among `count` threads (a multiple of 32) on hardware barrier `id`
 // (id 0 is __syncthreads).
@@ -332,15 +326,6 @@ FAB_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 
-FAB_DEV void tmem_st16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-
 FAB_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ----------------------------------------------------------------- math
@@ -399,16 +384,6 @@ FAB_DEV uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
   return v;
-}
-
-FAB_DEV float ld_shared_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-FAB_DEV void st_shared_f32(uint32_t addr, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // The first live tile and one past the last of a live-tile map row of n
