@@ -537,7 +537,8 @@ def run_fab(args, rank, world, local):
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+            "ms_step_median": round(statistics.median(step_ms), 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "M": w.M, "D": w.DK,
                        "causal": w.causal, "mask": w.mask, "seed": w.seed, "parallelism": f"replicas x{world}",
