@@ -22,7 +22,8 @@
 // then bounded by 2^8 and O is rescaled in tensor memory only on those rare
 // updates.  Using a stale max is exact: O and l share it.
 //
-// Warps (352 threads): 0 = TMA producer; 1 = tensor-memory allocator and S
+// Warps (384 threads): 0 = TMA producer (Q, key tiles); 11 = value-tile
+// producer; 1 = tensor-memory allocator and S
 // issuer; 10 = PV issuer (lane 0 of an issuer warp issues); 2-9 = softmax,
 // rescale and epilogue (thread = query row; two warps per tensor-memory lane
 // quarter, each taking 64 of a tile's 128 keys).  Causal and key-bound tests
@@ -42,7 +43,7 @@ __device__ uint32_t g_err_fwd;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
 
 template <int D, bool F16 = false>
@@ -77,7 +78,7 @@ struct FCfg {
 
 enum : int {
   F_Q = 0,       // phase k: unit k's Q landed
-  F_FULL = 1,    // + g % 3: K_g and V_g landed
+  F_FULL = 1,    // + g % 3: K_g landed
   F_S = 4,       // + g % 3: S(g) landed
   F_P = 7,       // + g % 3: softmax warps wrote P(g) (and rescaled O if they had to)
   F_PV = 10,     // + g % 3: PV(g) finished (its stage, S buffer free; O holds the unit's tiles <= g)
@@ -86,7 +87,8 @@ enum : int {
   F_QE = 15,     // phase k: unit k's S MMAs finished (Q free)
   F_OE = 16,     // phase k: unit k's epilogue read O from tensor memory
   F_STG = 17,    // phase k: unit k's O is staged in shared memory
-  F_COUNT = 18
+  F_VF = 18,     // + g % 3: V_g landed
+  F_COUNT = 21
 };
 
 struct FParams {
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(F_Q), 1);
     for (int s = 0; s < 3; ++s) {
       mbar_init(bar(F_FULL + s), 1);
+      mbar_init(bar(F_VF + s), 1);
       mbar_init(bar(F_S + s), 1);
       mbar_init(bar(F_P + s), kSoftmaxThreads);
       mbar_init(bar(F_PV + s), 1);
@@ -215,11 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Per unit: K_g, V_g of its first tile, its Q (once the previous unit's
-    // S MMAs are done with theirs), then the other tiles' K, V.  K_g, V_g go
-    // into stage g % 3 once PV(g-3) is done with it; g counts tiles across
-    // units.  A unit's epilogue stages O in the key tile of its last stage
-    // G % 3, so K_{G+3} also waits for that unit's bulk stores to read it.
+    // Per unit: K_g of its first tile, its Q (once the previous unit's S
+    // MMAs are done with theirs), then the other tiles' keys.  K_g goes into
+    // the key half of stage g % 3 once S(g-3) is done with it (the value
+    // tiles have a producer warp of their own, so a key load never waits
+    // behind a value tile's PV); g counts tiles across units.  A unit's
+    // epilogue stages O in the key tile of its last stage G % 3, so K_{G+3}
+    // also waits for that unit's bulk stores to read it.
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
@@ -233,18 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kvrow = x.b * (int)p.Hkv + x.hkv;
         for (int j = 0; j < x.nkv; ++j, ++g) {
           const int s = g % 3;
-          if (g >= 3 && !(ok = mbar_wait(bar(F_PV + s), ((g / 3) - 1) & 1, abort_flag, err))) break;
+          if (g >= 3 && !(ok = mbar_wait(bar(F_S + s), ((g / 3) - 1) & 1, abort_flag, err))) break;
 #pragma unroll
           for (int i = 0; i < 3; ++i)
             if (ok && stG[i] + 3 == g) ok = counter_wait(o_cnt, (uint32_t)(stK[i] + 1), abort_flag, err);
           if (!ok) break;
           fence_proxy_async_smem();
-          mbar_arrive_expect_tx(bar(F_FULL + s), 2 * C::TILE);
+          mbar_arrive_expect_tx(bar(F_FULL + s), C::TILE);
           const uint32_t sk = sbase + C::OFF_KV + 2 * s * C::TILE;
-          for (int a = 0; a < C::ATOMS; ++a) {
+          for (int a = 0; a < C::ATOMS; ++a)
             tma_load_3d(sk + a * C::ATOM, &tmK, bar(F_FULL + s), a * 64, (x.j0 + j) * C::BK, kvrow);
-            tma_load_3d(sk + C::TILE + a * C::ATOM, &tmV, bar(F_FULL + s), a * 64, (x.j0 + j) * C::BK, kvrow);
-          }
           ++issued;
           if (j == 0) {
             if (k > 0 && !(ok = mbar_wait(bar(F_QE), (k - 1) & 1, abort_flag, err))) break;
@@ -259,6 +262,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (q_issued > 0) mbar_drain(bar(F_Q), (q_issued - 1) & 1);
       for (int j = issued > 3 ? issued - 3 : 0; j < issued; ++j) mbar_drain(bar(F_FULL + j % 3), (j / 3) & 1);
+    }
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ value producer
+    // V_g into the value half of stage g % 3 once PV(g-3) is done with it
+    if (lane == 0) {
+      int g = 0, k = 0, issued = 0;
+      bool ok = true;
+      for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
+        const Unit x = unit_of(k);
+        const int kvrow = x.b * (int)p.Hkv + x.hkv;
+        for (int j = 0; j < x.nkv; ++j, ++g) {
+          const int s = g % 3;
+          if (g >= 3 && !(ok = mbar_wait(bar(F_PV + s), ((g / 3) - 1) & 1, abort_flag, err))) break;
+          mbar_arrive_expect_tx(bar(F_VF + s), C::TILE);
+          const uint32_t sv = sbase + C::OFF_KV + (2 * s + 1) * C::TILE;
+          for (int a = 0; a < C::ATOMS; ++a)
+            tma_load_3d(sv + a * C::ATOM, &tmV, bar(F_VF + s), a * 64, (x.j0 + j) * C::BK, kvrow);
+          ++issued;
+        }
+      }
+      for (int j = issued > 3 ? issued - 3 : 0; j < issued; ++j) mbar_drain(bar(F_VF + j % 3), (j / 3) & 1);
     }
   } else if (warp == 1 || warp == 10) {
     // ------------------------------------------------------------ MMA issuers
@@ -308,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < nkv; ++j, ++g) {
           const int s = g % 3;
           if (!(ok = wall(F_P + s, (g / 3) & 1))) break;
+          if (!(ok = wall(F_VF + s, (g / 3) & 1))) break;
           if (j == 0 && k > 0 && !(ok = wall(F_OE, (k - 1) & 1))) break;
           tc_fence_after();
           const uint32_t sV = sbase + C::OFF_KV + (2 * s + 1) * C::TILE;
