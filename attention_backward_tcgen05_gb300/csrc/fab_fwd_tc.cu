@@ -295,7 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     if (warp == 1) {
       // S(g) = Q K_g^T into buffer g % 3 once K_g landed and PV(g-3) is done
-      // with the buffer's P; after a unit's last S, its Q is free
+      // with the buffer's P; after a unit's last S, its Q is free.  A unit's
+      // second S also waits for the previous unit's last PV, which the
+      // softmax warps' epilogue waits for: issued behind the next unit's
+      // first two S products, that PV came ~500 cycles later
       const uint32_t sQ = sbase + C::OFF_Q;
       int g = 0, k = 0;
       for (int u = unit_at(0); ok && u < n_units; u = unit_at(++k)) {
@@ -305,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = g % 3;
           if (!(ok = wall(F_FULL + s, (g / 3) & 1))) break;
           if (g >= 3 && !(ok = wall(F_PV + s, ((g / 3) - 1) & 1))) break;
+          if (j == 1 && k > 0 && !(ok = wall(F_PV + (g - 2) % 3, ((g - 2) / 3) & 1))) break;
           tc_fence_after();
           const uint32_t sK = sbase + C::OFF_KV + 2 * s * C::TILE;
 #pragma unroll

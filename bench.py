@@ -14,8 +14,10 @@ host buffers (pinned H2D copies of the inputs, fab_backward, D2H of the
 packed gradients; once with the saved o and lse, once with the op's own
 operands q, k, v, the mask and d, the forward then recomputed inside), the
 forward kernel's TFLOP/s, fab_backward without o and lse on resident inputs,
-the two-phase API's D_i kernel in GB/s, and the fp64 CPU oracle on the
-workload's (batch, key/value head) units.
+the two-phase API's D_i kernel in GB/s (each of these three after at least
+three warm-up calls, the L2 flushed before every call, median of the timed
+calls), and the fp64 CPU oracle on the workload's (batch, key/value head)
+units.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl fab|reference]
 
@@ -284,17 +286,6 @@ def run_fab(args, rank, world, local):
     dt = binding.dtype_code(q)
     stream = torch.cuda.current_stream()
 
-    # forward once (saved O and LSE), timed on its own
-    o, lse = binding.forward(q, k, v, mask, w.causal, w.scale)
-    fwd_ms = []
-    for i in range(3 if args.forward_steps else 0):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        binding.fab_forward_lse(q, k, v, mask, w.causal, w.scale, o, lse)
-        e1.record(stream)
-        e1.synchronize()
-        fwd_ms.append(e0.elapsed_time(e1))
-
     ws, packed = binding.alloc_backward(dims, dt, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -304,6 +295,28 @@ def run_fab(args, rank, world, local):
         # lines leave L2 (written back to HBM) here, not inside the timed call
         flush.fill_(val)
         flush_rd.amax()
+
+    def time_calls(call, n_timed):
+        # the side measurements: untimed warm-up calls, then n_timed calls,
+        # each after an L2 flush, timed with CUDA events on the stream
+        n_warm = max(3, args.warmup)
+        ms = []
+        for i in range(n_warm + n_timed):
+            flush_l2(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= n_warm:
+                ms.append(e0.elapsed_time(e1))
+        return ms
+
+    # the forward (saved O and LSE), timed on its own
+    o, lse = binding.forward(q, k, v, mask, w.causal, w.scale)
+    fwd_ms = []
+    if args.forward_steps:
+        fwd_ms = time_calls(lambda: binding.fab_forward_lse(q, k, v, mask, w.causal, w.scale, o, lse), 10)
     tensor_core = w.dtype in ("bf16", "f16") and w.DK == w.DV and w.DK in (64, 128)
 
     # fab_backward without o and lse (the op's own operands only): the forward
@@ -311,30 +324,15 @@ def run_fab(args, rank, world, local):
     rec_ms = []
     if args.forward_steps:
         ws_r, packed_r = binding.alloc_backward(dims, dt, dev, recompute=True)
-        for i in range(4):
-            flush_l2(float(i))
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            binding.fab_backward(q, k, v, d, None, None, mask, w.causal, w.scale, ws_r, packed_r)
-            e1.record(stream)
-            e1.synchronize()
-            if i > 0:
-                rec_ms.append(e0.elapsed_time(e1))
+        rec_ms = time_calls(lambda: binding.fab_backward(q, k, v, d, None, None, mask, w.causal, w.scale,
+                                                         ws_r, packed_r), 5)
         del ws_r, packed_r
 
     # the two-phase API's D_i kernel (fab_backward computes D_i inside the
     # query pass instead): HBM-bound, timed on its own between L2 flushes
     pre_ms = []
     if args.forward_steps:
-        for i in range(4):
-            flush_l2(float(i))
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            binding.fab_backward_preprocess(d, o, dims, ws, packed)
-            e1.record(stream)
-            e1.synchronize()
-            if i > 0:
-                pre_ms.append(e0.elapsed_time(e1))
+        pre_ms = time_calls(lambda: binding.fab_backward_preprocess(d, o, dims, ws, packed), 5)
 
     def step():
         binding.fab_backward(q, k, v, d, o, lse, mask, w.causal, w.scale, ws, packed)
@@ -554,7 +552,7 @@ def run_fab(args, rank, world, local):
                           "note": "each entry point timed on its own, outside the timed region"},
             "wall_s": round(wall, 4),
             "forward": ({"tflops": round(forward_flops(w) / (statistics.median(fwd_ms) / 1e3) / 1e12, 2),
-                         "ms": round(statistics.median(fwd_ms), 3),
+                         "ms": round(statistics.median(fwd_ms), 4), "timed_calls": len(fwd_ms),
                          "kernel": "fwd_tc_kernel" if tensor_core else "fwd_simt_kernel"}
                         if fwd_ms else None),
             "preprocess": ({"gbps": round(preprocess_bytes(w) / (statistics.median(pre_ms) / 1e3) / 1e9, 1),
