@@ -37,6 +37,12 @@ SMALL = [
     ("tc64_causal", 2, 2, 2, 256, 256, 64, 64, "bf16", True, "none"),
     ("tc64_mask_gqa_ragged", 1, 4, 2, 70, 130, 64, 64, "bf16", False, "random"),
     ("tc128_single", 1, 1, 1, 1, 1, 128, 128, "bf16", False, "none"),
+    # eight query heads per key/value head (the key pass walks all eight for
+    # every query tile); one ragged query tile against eight key tiles; many
+    # query tiles against one ragged key tile
+    ("tc128_gqa8_causal", 1, 8, 1, 300, 300, 128, 128, "bf16", True, "none"),
+    ("tc64_short_q_long_k", 1, 2, 1, 64, 1000, 64, 64, "bf16", False, "none"),
+    ("tc128_long_q_short_k", 1, 2, 2, 1000, 64, 128, 128, "bf16", False, "none"),
     # more work units than SMs, so each persistent CTA walks several; causal
     # units of 1..5 tiles put short units back to back
     ("tc64_causal_many_units", 8, 8, 8, 640, 640, 64, 64, "bf16", True, "none"),
@@ -65,6 +71,7 @@ SMALL = [
     ("tc128_f16_causal_gqa_mask", 2, 4, 2, 200, 300, 128, 128, "f16", True, "random"),
     ("tc64_f16_mask_ragged", 1, 4, 2, 96, 130, 64, 64, "f16", False, "random"),
     ("tc128_f16_many_units", 16, 8, 4, 384, 384, 128, 128, "f16", True, "none"),
+    ("tc64_f16_causal_gqa", 2, 4, 2, 260, 260, 64, 64, "f16", True, "none"),
     ("simt_f16_odd", 1, 2, 1, 33, 47, 40, 24, "f16", False, "random"),
     # the pages' packing shape: widths below one 16-byte chunk, DK != DV
     ("simt_f32_dk3_dv5", 2, 4, 2, 37, 29, 3, 5, "f32", False, "random"),
