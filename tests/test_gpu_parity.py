@@ -96,6 +96,34 @@ def test_small_cases(case):
     check_pads_zero(w, gpu["packed"])
 
 
+def test_masked_units_past_the_span_table():
+    # more masked work units per CTA than the kernels' span tables hold (160
+    # units each): units past the table walk their whole tile range instead
+    # of the live span, which only adds exact zeros.  The padding mask makes
+    # the second key tile (keys 128, 129) and the last query rows all -inf.
+    # One query tile per head: the query pass and the forward run B*H =
+    # 24,576 units, the key pass B*Hkv*2 = 24,576, so every persistent CTA
+    # walks 161-162 units (152 SMs).
+    B, H, Hkv, N, M, D = 16, 1536, 768, 16, 130, 64
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert B * H > 160 * sms and B * Hkv * 2 > 160 * sms, "the shape no longer passes the span tables"
+    w = inputs.custom(B, H, Hkv, N, M, D, D, mask="pad", mask_p=0.05, seed=77, name="past_span_table")
+    x = inputs.make(w)
+    gpu = run_gpu(w, x)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    # o and lse NULL: the forward inside fab_backward walks its span table too
+    recomputed = binding.backward(g["q"], g["k"], g["v"], g["d"], None, None, g["mask"], w.causal, w.scale)
+    torch.cuda.synchronize()
+    assert binding.fab_last_device_error() == binding.FAB_OK
+    assert np.array_equal(recomputed.to("cpu", torch.float64).numpy(), gpu["packed"])
+    del g, recomputed
+    ref = oracle_ref(w, x)
+    errs = compare(w, gpu, ref)
+    for key in ("dq", "dk", "dv", "o"):
+        assert errs[key] <= TOL["bf16"], (key, errs)
+    check_pads_zero(w, gpu["packed"])
+
+
 def test_unattended_keys_and_masked_rows_exact_zero():
     # causal with N < M leaves keys >= N unattended (a whole key tile of them);
     # a fully masked query row must get dQ exactly 0
